@@ -1,0 +1,332 @@
+"""Benchmark: 3D-RoPE full spatiotemporal attention on the Wan-14B 720p shape (B=2, 40 heads,
+d=128, latent grid 21x45x80 = 75600 tokens, bf16), one call = one step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Prints one JSON line.  `value` is achieved TFLOP/s (4*B*H*N^2*d per call) summed over ranks,
+timed with CUDA events on the launching stream over K back-to-back calls whose inputs are
+already resident in HBM (each of q, k, v is 1.55 GB, far larger than the 129 MB L2, so no L2
+flush is needed).  `e2e` times the same call through the public API with the inputs copied
+from pinned host memory and the output and lse copied back inside the timed region.  With
+N > 1 (torchrun) every rank runs an independent replica of the whole workload.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of rows instead.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from video_diffusion_transformer_rope_gb300 import configs, synth  # noqa: E402
+
+KERNEL_SRC = os.path.join(ROOT, "video_diffusion_transformer_rope_gb300", "csrc", "attn_fwd_sm103.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_bf16_sm103_traffic.txt")
+METRIC = "3D-RoPE attention TFLOP/s (4*B*H*N^2*d per call), Wan-14B 720p shape, 1 GB300"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk.get("bf16_tflops_sustained", 0) or 0), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+def _source_hash():
+    import hashlib
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _traffic_per_launch(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    key, val = line.split(":", 1)
+                    kv[key.strip()] = val.strip()
+        if kv.get("kernel_source_sha256_16") != _source_hash() or kv.get("workload") != workload:
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.out,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _cpu_oracle_sample(w, q, k, v, heads, rows_per_head, seed=0):
+    """Time the oracle (as it stands) on rows_per_head query rows of `heads` (b, h) pairs.
+    Inputs are already on the host.  Returns (seconds, rows)."""
+    import numpy as np
+    import oracle.fp64 as O
+    rng = np.random.default_rng(seed)
+    rows = []
+    for i in range(heads):
+        b, h = (i % w.B), (i * 7) % w.H
+        for n in rng.choice(w.N, rows_per_head, replace=False):
+            rows.append((b, h, int(n)))
+    t0 = time.perf_counter()
+    O.rope3d_attention_rows(q, k, v, (w.T, w.Hg, w.Wg), rows, w.sections, w.theta)
+    return time.perf_counter() - t0, len(rows)
+
+
+def run_reference(args, w):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import torch
+    if torch.cuda.is_available():    # the seeded draw is faster on a device; values go to the host
+        q, k, v = (t.cpu() for t in synth.make_qkv(w, device="cuda"))
+    else:
+        q, k, v = synth.make_qkv(w, device="cpu")
+    flops_per_row = 4.0 * w.N * w.d
+    heads, rph = 2, 32
+    for _ in range(args.warmup):
+        _cpu_oracle_sample(w, q, k, v, heads, rph)
+    times = []
+    rows = 0
+    for s in range(args.steps):
+        dt, rows = _cpu_oracle_sample(w, q, k, v, heads, rph, seed=s)
+        times.append(dt)
+    per_step = sum(times) / len(times)
+    tflops = flops_per_row * rows / per_step / 1e12
+    full_ms = w.flops / (tflops * 1e12) * 1e3
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": full_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), bf16-rounded)",
+        "config": _config(w),
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} query rows ({heads} heads x {rph}) of the full workload "
+                                   f"per step, fp64 NumPy, extrapolated to a full call "
+                                   f"({per_step:.2f} s per sample)"},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(w):
+    return {"workload": w.name, "B": w.B, "heads": w.H, "head_dim": w.d,
+            "grid": f"{w.T}x{w.Hg}x{w.Wg}", "N": w.N,
+            "sections": "/".join(map(str, w.sections)), "theta": w.theta,
+            "l2": "inputs larger than L2 (q, k, v 1.55 GB each); no flush",
+            "parallelism": "replicas (one independent call per GPU)"}
+
+
+def run_ours(args, w):
+    import torch
+    import video_diffusion_transformer_rope_gb300 as vdx
+    from video_diffusion_transformer_rope_gb300 import _build
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    if rank == 0:
+        _build.build()
+    if ws > 1:
+        torch.distributed.barrier()
+    vdx.lib()
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    q, k, v = synth.make_qkv(w, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    grid = (w.T, w.Hg, w.Wg)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        vdx.rope3d_attn(q, k, v, grid, w.sections, w.theta, out=out, lse=lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    vdx.sync_check(stream)
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if ws == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- device-resident timed region
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    try:
+        smi_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        smi_id = str(dev.index)
+    with ClockSampler(smi_id) as clk:
+        barrier()
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        barrier()
+    vdx.sync_check(stream)
+    ms = max_over_ranks(start.elapsed_time(end) / args.steps)
+    clocks = clk.summary()
+
+    # ---- end to end through the public API: pinned host inputs in, out + lse back out
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    e2e_steps = max(1, min(args.steps, 5))
+    barrier()
+    start.record(stream)
+    for _ in range(e2e_steps):
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+    end.record(stream)
+    barrier()
+    vdx.sync_check(stream)
+    e2e_ms = max_over_ranks(start.elapsed_time(end) / e2e_steps)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+
+    tflops_rank = w.flops / (ms * 1e-3) / 1e12
+    value = ws * w.flops / (ms * 1e-3) / 1e12
+    e2e_value = ws * w.flops / (e2e_ms * 1e-3) / 1e12
+    peak, peak_sus, peak_src = _peaks()
+    traffic = _traffic_per_launch(w.name)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        hq64, hk64, hv64 = hq, hk, hv
+        heads, rph = 4, 64
+        dt, rows = _cpu_oracle_sample(w, hq64, hk64, hv64, heads, rph)
+        cpu_tf = 4.0 * w.N * w.d * rows / dt / 1e12
+        cpu = {"value": cpu_tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{rows} query rows ({heads} heads x {rph}) of this workload, fp64 NumPy "
+                         f"oracle, {dt:.1f} s, extrapolated to TFLOP/s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) on device, bf16)",
+            "config": _config(w),
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "roofline": {"bound": "tensor", "achieved": tflops_rank, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops_rank / peak, "traffic": traffic,
+                         "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)",
+                         "frac_of_sustained": (tflops_rank / peak_sus) if peak_sus else None,
+                         "kernel": "attn_fwd_bf16_sm103"},
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=configs.WAN14B_720P.name, choices=sorted(configs.BY_NAME))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = configs.BY_NAME[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

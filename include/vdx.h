@@ -1,0 +1,84 @@
+/* vdx — 3D-RoPE full spatiotemporal self-attention for video diffusion transformers, on one
+ * GB300 (sm_103a).
+ *
+ * Operation (vidax: A Unified JAX Framework for Video Generative Models on Accelerator
+ * Meshes, §2 "3D RoPE, 3D VAEs, and flash attention": rotary 3D position embedding on Q and
+ * K, then attention that never materialises the N x N score matrix; §1 "Motivation and gap":
+ * tens of thousands of latent-patch tokens).  For batch b, head h, query token n:
+ *
+ *     q'_n  = R(n) q_n,   k'_m = R(m) k_m
+ *     lse_n = log sum_m exp(scale * <q'_n, k'_m>)           (natural log, all m: non-causal)
+ *     out_n = sum_m exp(scale * <q'_n, k'_m> - lse_n) v_m
+ *
+ * R(n) rotates adjacent channel pairs (2i, 2i+1) like a complex number times exp(i*angle).
+ * head_dim d is split into three rotary sections, in this order: sec_t dims turning with the
+ * frame index t, sec_h with the grid row h, sec_w with the grid column w.  Within a section of
+ * S dims, pair j turns at angle pos * theta^(-2j/S).  Token n = t*Hgrid*Wgrid + h*Wgrid + w.
+ *
+ * Layouts (row-major, contiguous):
+ *   q, k, v, out : [B, N, H, d]   with N = T*Hgrid*Wgrid
+ *   lse          : [B, H, N]      float32, may be NULL
+ *
+ * Ownership: every pointer is a device pointer owned by the caller.  The library owns only a
+ * per-device cache of cos/sin tables (one per distinct grid/sections/theta; built on the
+ * first call with that key, which allocates and uploads synchronously) and an error word;
+ * vdx_shutdown() frees the tables.  Calls are asynchronous on `stream` (a cudaStream_t; NULL
+ * means the legacy default stream).
+ *
+ * Errors: argument problems are reported before anything is launched and return a non-zero
+ * vdx_status; vdx_last_error() gives a message (per host thread).  Device-side problems (a
+ * pipeline wait that gave up after 1 s) are latched in a device error word read and cleared
+ * by vdx_sync_check().
+ */
+#ifndef VDX_H_
+#define VDX_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  VDX_OK = 0,
+  VDX_ERR_ARG = 1,          /* bad size, section split, NULL pointer, aliasing        */
+  VDX_ERR_ALIGN = 2,        /* a pointer is not 16-byte aligned                       */
+  VDX_ERR_UNSUPPORTED = 3,  /* valid, but outside what this build implements          */
+  VDX_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed                      */
+  VDX_ERR_TIMEOUT = 5       /* a kernel pipeline wait gave up (see vdx_sync_check)    */
+} vdx_status;
+
+/* bf16 path, tcgen05 tensor cores.  q, k, v, out: __nv_bfloat16 [B, N, H, d]; d must be 128.
+ * sec_t/sec_h/sec_w: even, sum to d; all three 0 selects d - 4*(d/6), 2*(d/6), 2*(d/6)
+ * (44/42/42 at d = 128).  scale <= 0 selects 1/sqrt(d).  theta > 0 (10000 for Wan).
+ * out must not overlap q, k or v.  B, H, T, Hgrid, Wgrid >= 1. */
+vdx_status vdx_rope3d_attn(const void* q, const void* k, const void* v, void* out, float* lse,
+                           int B, int H, int T, int Hgrid, int Wgrid, int d,
+                           int sec_t, int sec_h, int sec_w, double theta, float scale,
+                           void* stream);
+
+/* fp32 path (CUDA cores, fp32 arithmetic throughout).  Same operation and rules; q, k, v,
+ * out are float [B, N, H, d]; d must be 64 or 128. */
+vdx_status vdx_rope3d_attn_f32(const float* q, const float* k, const float* v, float* out,
+                               float* lse, int B, int H, int T, int Hgrid, int Wgrid, int d,
+                               int sec_t, int sec_h, int sec_w, double theta, float scale,
+                               void* stream);
+
+/* Synchronise `stream`, then read and clear the device error word.  Returns VDX_OK,
+ * VDX_ERR_TIMEOUT (a kernel gave up on a pipeline wait; the output of that call is
+ * undefined) or VDX_ERR_CUDA (an asynchronous CUDA error is pending). */
+vdx_status vdx_sync_check(void* stream);
+
+/* Message for the last non-OK status returned on this host thread ("" if none). */
+const char* vdx_last_error(void);
+
+/* Free every cached cos/sin table on every device.  Not to be called while work that uses
+ * them is in flight. */
+void vdx_shutdown(void);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int vdx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VDX_H_ */

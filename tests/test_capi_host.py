@@ -1,0 +1,78 @@
+"""The C-ABI library: loads without a GPU, exports every symbol include/vdx.h declares, and
+rejects bad arguments before touching CUDA (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import video_diffusion_transformer_rope_gb300 as vdx
+from video_diffusion_transformer_rope_gb300 import _binding, _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return vdx.lib()
+
+
+def _declared():
+    hdr = open(os.path.join(ROOT, "include", "vdx.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    return set(re.findall(r"^\s*(?:vdx_status|const char\s*\*|void|int)\s+(vdx_\w+)\s*\(", hdr, re.M))
+
+
+def test_exports_every_declared_symbol(L):
+    decl = _declared()
+    assert decl == {"vdx_rope3d_attn", "vdx_rope3d_attn_f32", "vdx_sync_check", "vdx_last_error",
+                    "vdx_shutdown", "vdx_version"} | (decl - {"vdx_rope3d_attn", "vdx_rope3d_attn_f32",
+                                                              "vdx_sync_check", "vdx_last_error",
+                                                              "vdx_shutdown", "vdx_version"})
+    for name in decl:
+        assert hasattr(L, name), name
+    assert set(_binding.SIGNATURES) == decl
+    assert L.vdx_version() == 100
+
+
+FAKE = 0x7f0000000000          # 16-byte aligned, never dereferenced: every call below fails first
+
+
+def _call(L, fn="vdx_rope3d_attn", q=FAKE, k=FAKE + (1 << 32), v=FAKE + (2 << 32),
+          out=FAKE + (3 << 32), lse=0, B=1, H=2, T=2, Hg=3, Wg=4, d=128, st=0, sh=0, sw=0,
+          theta=10000.0, scale=0.0):
+    return getattr(L, fn)(ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v),
+                          ctypes.c_void_p(out), ctypes.c_void_p(lse), B, H, T, Hg, Wg, d,
+                          st, sh, sw, theta, scale, None)
+
+
+@pytest.mark.parametrize("kw,status,msg", [
+    (dict(d=64), _binding.VDX_ERR_UNSUPPORTED, "head_dim 128"),
+    (dict(fn="vdx_rope3d_attn_f32", d=96), _binding.VDX_ERR_UNSUPPORTED, "64 or 128"),
+    (dict(q=0), _binding.VDX_ERR_ARG, "non-NULL"),
+    (dict(out=0), _binding.VDX_ERR_ARG, "non-NULL"),
+    (dict(B=0), _binding.VDX_ERR_ARG, ">= 1"),
+    (dict(Wg=-3), _binding.VDX_ERR_ARG, ">= 1"),
+    (dict(st=44, sh=42, sw=41), _binding.VDX_ERR_ARG, "sections"),
+    (dict(st=43, sh=43, sw=42), _binding.VDX_ERR_ARG, "sections"),
+    (dict(st=40, sh=40, sw=40), _binding.VDX_ERR_ARG, "sum to d"),
+    (dict(theta=0.0), _binding.VDX_ERR_ARG, "theta"),
+    (dict(theta=-1.0), _binding.VDX_ERR_ARG, "theta"),
+    (dict(scale=float("nan")), _binding.VDX_ERR_ARG, "scale"),
+    (dict(k=FAKE + 8), _binding.VDX_ERR_ALIGN, "aligned"),
+    (dict(lse=FAKE + (4 << 32) + 4), _binding.VDX_ERR_ALIGN, "aligned"),
+    (dict(out=FAKE + 64), _binding.VDX_ERR_ARG, "overlaps"),
+    (dict(lse=FAKE + (1 << 32) + 4096), _binding.VDX_ERR_ARG, "overlaps"),
+    (dict(T=100000, Hg=1000, Wg=1000), _binding.VDX_ERR_ARG, "too large"),
+])
+def test_rejects_bad_arguments_without_cuda(L, kw, status, msg):
+    assert _call(L, **kw) == status
+    assert msg in L.vdx_last_error().decode()
+
+
+def test_python_binding_rejects_mismatched_grid(L):
+    import torch
+    q = torch.zeros(1, 10, 1, 128)
+    with pytest.raises(vdx.VdxError):
+        vdx.rope3d_attn(q, q, q, (2, 2, 2))

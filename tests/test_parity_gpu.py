@@ -1,0 +1,129 @@
+"""GPU path (through the C ABI) against the fp64 oracle, element by element on the same seeded
+inputs.  Tolerances: fp32 path max-abs <= 1e-4; bf16 path out max-abs <= 2e-2, out mean-abs
+<= 2e-3, lse max-abs <= 1e-3 (full comparison at small sizes, sampled rows at full size)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.fp64 as O
+import video_diffusion_transformer_rope_gb300 as vdx
+from video_diffusion_transformer_rope_gb300 import configs, synth
+
+pytestmark = pytest.mark.gpu
+
+F32_TOL = 1e-4
+BF16_MAX, BF16_MEAN, LSE_TOL = 2e-2, 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from video_diffusion_transformer_rope_gb300 import _build
+    _build.build()
+    vdx.lib()
+
+
+def _run(w, q, k, v):
+    out, lse = vdx.rope3d_attn(q, k, v, (w.T, w.Hg, w.Wg), w.sections, w.theta)
+    vdx.sync_check()
+    return out, lse
+
+
+def _full_compare(w, dev_qkv=None):
+    q, k, v = dev_qkv if dev_qkv is not None else (t.cuda() for t in synth.make_qkv(w))
+    out, lse = _run(w, q, k, v)
+    ref_o, ref_l = O.rope3d_attention(q, k, v, (w.T, w.Hg, w.Wg), w.sections, w.theta)
+    got_o = out.double().cpu().numpy()
+    got_l = lse.double().cpu().numpy()
+    err = np.abs(got_o - ref_o)
+    return err.max(), err.mean(), np.abs(got_l - ref_l).max()
+
+
+def test_tiny_f32_config():
+    mx, mean, lerr = _full_compare(configs.TINY_F32)
+    assert mx <= F32_TOL and lerr <= F32_TOL, (mx, lerr)
+
+
+@pytest.mark.parametrize("grid,d", [((3, 8, 8), 128), ((2, 9, 13), 64), ((1, 1, 1), 64),
+                                    ((2, 1, 67), 128)])
+def test_f32_shapes(grid, d):
+    w = dataclasses.replace(configs.TINY_F32, T=grid[0], Hg=grid[1], Wg=grid[2], d=d,
+                            sections=O.default_sections(d), B=2, H=3, seed=11)
+    mx, mean, lerr = _full_compare(w)
+    assert mx <= F32_TOL and lerr <= F32_TOL, (mx, lerr)
+
+
+# Small bf16 shapes spanning several 128-key tiles, 256-row CTAs and ragged tails:
+# N = 192 (tail 64), 105 (< one tile), 1, 129 (= 1 mod 128), 468, 640 (exact), T=1, Wg=1.
+BF16_GRIDS = [(3, 8, 8), (3, 5, 7), (1, 1, 1), (1, 1, 129), (4, 9, 13), (5, 8, 16), (1, 16, 24),
+              (7, 40, 1)]
+
+
+@pytest.mark.parametrize("grid", BF16_GRIDS, ids=lambda g: "x".join(map(str, g)))
+def test_bf16_small_shapes(grid):
+    w = dataclasses.replace(configs.WAN13B_480P, B=2, H=3, T=grid[0], Hg=grid[1], Wg=grid[2], seed=21)
+    mx, mean, lerr = _full_compare(w)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
+
+
+def test_bf16_custom_sections_theta_scale():
+    w = dataclasses.replace(configs.WAN13B_480P, B=1, H=2, T=3, Hg=6, Wg=20, sections=(64, 32, 32),
+                            theta=500.0, seed=22)
+    q, k, v = (t.cuda() for t in synth.make_qkv(w))
+    out, lse = vdx.rope3d_attn(q, k, v, (3, 6, 20), w.sections, w.theta, scale=0.05)
+    vdx.sync_check()
+    ref_o, ref_l = O.rope3d_attention(q, k, v, (3, 6, 20), w.sections, w.theta, scale=0.05)
+    assert np.abs(out.double().cpu().numpy() - ref_o).max() <= BF16_MAX
+    assert np.abs(lse.double().cpu().numpy() - ref_l).max() <= LSE_TOL
+
+
+def test_bf16_large_logits_small():
+    w = dataclasses.replace(configs.LONG_STRESS, B=1, H=4, T=2, Hg=9, Wg=40, seed=23)
+    mx, mean, lerr = _full_compare(w)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
+
+
+def test_bf16_deterministic_and_guard_bands():
+    w = dataclasses.replace(configs.WAN13B_480P, B=1, H=2, T=2, Hg=10, Wg=13, seed=24)
+    q, k, v = (t.cuda() for t in synth.make_qkv(w))
+    numel = q.numel()
+    guard = 4096
+    buf = torch.full((numel + 2 * guard,), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[guard:guard + numel].view_as(q)
+    lbuf = torch.full((w.B * w.H * w.N + 2 * guard,), -3.0, dtype=torch.float32, device="cuda")
+    lse = lbuf[guard:guard + w.B * w.H * w.N].view(w.B, w.H, w.N)
+    vdx.rope3d_attn(q, k, v, (w.T, w.Hg, w.Wg), out=out, lse=lse)
+    vdx.sync_check()
+    first = out.clone(), lse.clone()
+    vdx.rope3d_attn(q, k, v, (w.T, w.Hg, w.Wg), out=out, lse=lse)
+    vdx.sync_check()
+    assert torch.equal(first[0], out) and torch.equal(first[1], lse)
+    assert torch.all(buf[:guard] == 7.0) and torch.all(buf[guard + numel:] == 7.0)
+    assert torch.all(lbuf[:guard] == -3.0) and torch.all(lbuf[guard + w.B * w.H * w.N:] == -3.0)
+    out2, none = vdx.rope3d_attn(q, k, v, (w.T, w.Hg, w.Wg), return_lse=False)
+    vdx.sync_check()
+    assert none is None and torch.equal(out2, out)
+
+
+def _sampled_compare(w, rows=512):
+    q, k, v = synth.make_qkv(w, device="cuda")
+    out, lse = _run(w, q, k, v)
+    sel = synth.sample_rows(w, rows)
+    ref_o, ref_l = O.rope3d_attention_rows(q, k, v, (w.T, w.Hg, w.Wg), sel, w.sections, w.theta)
+    b = torch.tensor([r[0] for r in sel], device="cuda")
+    h = torch.tensor([r[1] for r in sel], device="cuda")
+    n = torch.tensor([r[2] for r in sel], device="cuda")
+    got_o = out[b, n, h].double().cpu().numpy()
+    got_l = lse[b, h, n].double().cpu().numpy()
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    err = np.abs(got_o - ref_o)
+    return err.max(), err.mean(), np.abs(got_l - ref_l).max()
+
+
+@pytest.mark.parametrize("w", [configs.WAN13B_480P, configs.WAN14B_480P, configs.WAN14B_720P,
+                               configs.LONG_STRESS], ids=lambda w: w.name)
+def test_full_size_configs_sampled(w):
+    mx, mean, lerr = _sampled_compare(w)
+    print(f"{w.name}: out max {mx:.3e} mean {mean:.3e} lse max {lerr:.3e}")
+    assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)

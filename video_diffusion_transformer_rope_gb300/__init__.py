@@ -1,0 +1,6 @@
+"""vdx: 3D-RoPE full spatiotemporal self-attention for video diffusion transformers on one
+GB300 (sm_103a).  The computation lives in libvdx.so (C ABI, include/vdx.h); this package
+holds the ctypes binding, the build step, the measured workloads and the seeded input recipe.
+"""
+from ._binding import (VdxError, lib, rope3d_attn, sync_check, shutdown, version,  # noqa: F401
+                       SIGNATURES, LIB_PATH)

@@ -1,0 +1,109 @@
+"""ctypes binding of libvdx.so (include/vdx.h).  Argument marshalling only: every step of the
+computation runs in the library's CUDA kernels.  There is no fallback: if the library is not
+built, or a call fails, this raises.
+"""
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libvdx.so")
+
+VDX_OK, VDX_ERR_ARG, VDX_ERR_ALIGN, VDX_ERR_UNSUPPORTED, VDX_ERR_CUDA, VDX_ERR_TIMEOUT = range(6)
+STATUS_NAMES = {0: "VDX_OK", 1: "VDX_ERR_ARG", 2: "VDX_ERR_ALIGN", 3: "VDX_ERR_UNSUPPORTED",
+                4: "VDX_ERR_CUDA", 5: "VDX_ERR_TIMEOUT"}
+
+_p, _i, _d, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_float
+# name -> (restype, argtypes); mirrors include/vdx.h
+SIGNATURES = {
+    "vdx_rope3d_attn": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f, _p]),
+    "vdx_rope3d_attn_f32": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f, _p]),
+    "vdx_sync_check": (_i, [_p]),
+    "vdx_last_error": (ctypes.c_char_p, []),
+    "vdx_shutdown": (None, []),
+    "vdx_version": (_i, []),
+}
+
+_lib = None
+
+
+class VdxError(RuntimeError):
+    def __init__(self, status, message):
+        self.status = status
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+
+
+def lib():
+    """Load libvdx.so once; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "video_diffusion_transformer_rope_gb300._build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status):
+    if status != VDX_OK:
+        raise VdxError(status, lib().vdx_last_error().decode())
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def rope3d_attn(q, k, v, grid, sections=(0, 0, 0), theta=10000.0, scale=0.0, out=None,
+                lse=None, return_lse=True, stream=None):
+    """3D-RoPE attention of CUDA tensors q, k, v laid out [B, N, H, d] (bf16 with d = 128, or
+    float32 with d = 64/128).  grid = (T, Hgrid, Wgrid) with N = T*Hgrid*Wgrid.
+
+    Returns (out [B, N, H, d] in the input dtype, lse [B, H, N] float32 or None).  Enqueued on
+    `stream` (default: torch's current stream); call sync_check() to surface device errors.
+    """
+    import torch
+    T, Hg, Wg = (int(x) for x in grid)
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise VdxError(VDX_ERR_ARG, f"q, k, v must share one [B, N, H, d] shape, got "
+                                    f"{tuple(q.shape)}, {tuple(k.shape)}, {tuple(v.shape)}")
+    B, N, H, d = q.shape
+    if N != T * Hg * Wg:
+        raise VdxError(VDX_ERR_ARG, f"N={N} does not match grid {T}x{Hg}x{Wg}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype:
+            raise VdxError(VDX_ERR_ARG, f"{name} must be a contiguous CUDA tensor of dtype {q.dtype}")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    st, sh, sw = (int(x) for x in sections)
+    args = (ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+            ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr() if lse is not None else 0),
+            B, H, T, Hg, Wg, d, st, sh, sw, float(theta), float(scale), _stream_handle(stream))
+    if q.dtype == torch.bfloat16:
+        _check(lib().vdx_rope3d_attn(*args))
+    elif q.dtype == torch.float32:
+        _check(lib().vdx_rope3d_attn_f32(*args))
+    else:
+        raise VdxError(VDX_ERR_UNSUPPORTED, f"dtype {q.dtype} (use bfloat16 or float32)")
+    return out, lse
+
+
+def sync_check(stream=None):
+    """Synchronise the stream and raise VdxError if a kernel reported a device-side problem."""
+    _check(lib().vdx_sync_check(_stream_handle(stream)))
+
+
+def shutdown():
+    lib().vdx_shutdown()
+
+
+def version():
+    return lib().vdx_version()

@@ -1,0 +1,538 @@
+// Warp-specialised flash-attention forward with fused 3D RoPE for sm_103a (GB300).
+//
+// Operation: vidax: A Unified JAX Framework for Video Generative Models on Accelerator
+// Meshes, §2 "3D RoPE, 3D VAEs, and flash attention" (rotary 3D positions on Q and K, then
+// attention without materialising the N x N scores).  bf16 in/out, d = 128, fp32 softmax
+// statistics and accumulators.
+//
+// One CTA owns 256 query rows (two 128-row Q tiles) of one (batch, head) and streams every
+// 128-key K/V tile of that head:
+//
+//   warps 0-3   softmax for Q tile 0   (thread = one query row = one TMEM lane)
+//   warps 4-7   softmax for Q tile 1
+//   warps 8-11  RoPE: rotate Q tiles once, and each K tile in shared memory as it lands
+//   warp  12    TMA producer: Q tiles once, then K/V tiles into two 2-stage rings
+//   warp  13    tcgen05 MMA issuer (one thread) and TMEM owner
+//   warps 14-15 idle
+//
+// TMEM (512 columns x 128 lanes, fp32): S0 [0,128)  S1 [128,256)  O0 [256,384)  O1 [384,512).
+// P_i (bf16, two per column) overwrites the first 64 columns of S_i and is the A operand of
+// the PV MMA straight from TMEM.  MMA issue order per key tile j:
+//     S0(j) = Q0 K_j^T ;  O1 += P1(j-1) V_{j-1} ;  S1(j) = Q1 K_j^T ;  O0 += P0(j) V_j
+// so softmax of one Q tile overlaps the tensor-core work of the other.  The online softmax
+// works in the log2 domain (exp2 with scale*log2(e) folded into one FMA) and only rescales
+// O when a row maximum grows by more than 8 (a factor 256), which keeps P <= 256.
+//
+// Shared memory: Q 2x32 KB, K ring 2x32 KB, V ring 2x32 KB, each tile stored as two
+// 128-row x 128-byte halves in the 128-byte-swizzled layout TMA writes; the cos/sin table
+// (when it fits) and the mbarriers follow.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+#include <cmath>
+
+#include "sm103_ptx.cuh"
+#include "vdx_internal.h"
+
+namespace vdx {
+namespace {
+
+constexpr int kBM = 128;                 // rows per Q tile
+constexpr int kQTiles = 2;               // Q tiles per CTA
+constexpr int kRowsPerCta = kBM * kQTiles;
+constexpr int kBN = 128;                 // keys per K/V tile
+constexpr int kD = 128;
+constexpr int kKStages = 2;
+constexpr int kVStages = 2;
+constexpr int kTileBytes = kBN * kD * 2; // 32 KB
+constexpr int kHalfBytes = kTileBytes / 2;
+constexpr int kThreads = 512;
+constexpr int kTmemCols = 512;
+
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kQTiles * kTileBytes;
+constexpr int kOffV = kOffK + kKStages * kTileBytes;
+constexpr int kOffTab = kOffV + kVStages * kTileBytes;
+constexpr int kMaxDynSmem = 232448;      // sm_100-family opt-in limit per CTA
+
+// Wait sites recorded in the error word when a bounded wait gives up.
+enum : int {
+  kSiteQFull = 1, kSiteKFull, kSiteKReady, kSiteKEmpty, kSiteVFull, kSiteVEmpty,
+  kSiteSFull, kSitePReady, kSiteQReady, kSiteOFinal, kSiteDrain
+};
+
+struct Ctl {
+  uint64_t q_full[kQTiles];
+  uint64_t q_ready[kQTiles];
+  uint64_t k_full[kKStages];
+  uint64_t k_ready[kKStages];
+  uint64_t k_empty[kKStages];
+  uint64_t v_full[kVStages];
+  uint64_t v_empty[kVStages];
+  uint64_t s_full[kQTiles];
+  uint64_t p_ready[kQTiles];
+  uint64_t o_final;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct Params {
+  int B, H, N, Hg, Wg, HgWg;
+  int half_t, half_h, half_w;
+  int off_h, off_w;            // table offsets of the h and w blocks (entries)
+  int table_entries;
+  int table_in_smem;
+  int n_qblk;                  // CTAs per (b, h)
+  int ctl_off;                 // byte offset of Ctl in the aligned dynamic smem
+  float scale_log2;            // scale * log2(e)
+  const float2* table;
+  __nv_bfloat16* out;
+  float* lse;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Bounded wait used on the way out: ignores the abort flag so that copies / MMAs that are
+// still in flight finish before shared or tensor memory is released.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return;
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(&g_error_word, 0u, 1u | (static_cast<unsigned>(kSiteDrain) << 8));
+      return;
+    }
+  }
+}
+
+// S(tmem) = A(smem, 128 x 128, K-major) * B(smem, 128 x 128, K-major)^T in 8 steps of K=16.
+// Each operand is two 16 KB halves (channels 0-63, 64-127); inside a 128-byte swizzled
+// half, K step kk starts 32 bytes further on.
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
+                                         uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+    mma_ss(d_tmem, smem_desc_sw128(a_smem + off, 16, 1024),
+           smem_desc_sw128(b_smem + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O(tmem) (+)= P(tmem, 128 x 128 bf16) * V(smem, 128 keys x 128 channels, channel-contiguous).
+// V is the MN-major B operand: 64-channel halves 16 KB apart (leading offset), 8-key groups
+// 1 KB apart (stride offset); K step kk covers keys 16kk..16kk+15 = 2 KB further on.
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk) {
+    mma_ts(d_tmem, p_tmem + kk * 8, smem_desc_sw128(v_smem + kk * 2048, kHalfBytes, 1024), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+// Rotate one 128-row tile in place (bf16, swizzled halves).  Thread t of the 128 RoPE
+// threads always touches 16-byte chunk (t & 15) of rows (t >> 4) + 8*it, so its four rotary
+// pairs, and therefore their axes and table columns, are fixed.
+struct RopeLane {
+  int tab_base[4];   // entry of position 0 for each of the thread's pairs
+  int tab_stride[4]; // entries per position step on that pair's axis
+  int axis[4];       // 0 = t, 1 = h, 2 = w
+  uint32_t chunk_off;
+  int rsub;
+};
+
+__device__ __forceinline__ RopeLane make_rope_lane(const Params& p, int t) {
+  RopeLane L;
+  const int c16 = t & 15;
+  const int half = c16 >> 3;
+  const int cc = c16 & 7;
+  L.rsub = t >> 4;
+  L.chunk_off = half * kHalfBytes + L.rsub * 128 + ((cc ^ L.rsub) << 4);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int pr = half * 32 + cc * 4 + e;
+    if (pr < p.half_t) {
+      L.axis[e] = 0; L.tab_base[e] = pr; L.tab_stride[e] = p.half_t;
+    } else if (pr < p.half_t + p.half_h) {
+      L.axis[e] = 1; L.tab_base[e] = p.off_h + (pr - p.half_t); L.tab_stride[e] = p.half_h;
+    } else {
+      L.axis[e] = 2; L.tab_base[e] = p.off_w + (pr - p.half_t - p.half_h);
+      L.tab_stride[e] = p.half_w;
+    }
+  }
+  return L;
+}
+
+__device__ __forceinline__ void rope_tile(const Params& p, const RopeLane& L, uint8_t* tile,
+                                          int n_first, const float2* __restrict__ tab) {
+  int n = n_first + L.rsub;
+  if (n >= p.N) return;
+  int pt = n / p.HgWg;
+  int rem = n - pt * p.HgWg;
+  int ph = rem / p.Wg;
+  int pw = rem - ph * p.Wg;
+#pragma unroll 2
+  for (int it = 0; it < kBM / 8; ++it) {
+    if (n >= p.N) break;
+    uint4* ptr = reinterpret_cast<uint4*>(tile + L.chunk_off + it * 1024);
+    uint4 x = *ptr;
+    uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int pos = L.axis[e] == 0 ? pt : (L.axis[e] == 1 ? ph : pw);
+      const float2 cs = tab[L.tab_base[e] + pos * L.tab_stride[e]];
+      __nv_bfloat162 v2 = *reinterpret_cast<__nv_bfloat162*>(&w[e]);
+      const float x0 = __low2float(v2), x1 = __high2float(v2);
+      const float y0 = fmaf(x0, cs.x, -x1 * cs.y);
+      const float y1 = fmaf(x0, cs.y, x1 * cs.x);
+      w[e] = pack_bf16x2(y0, y1);
+    }
+    *ptr = make_uint4(w[0], w[1], w[2], w[3]);
+    n += 8;
+    pw += 8;
+    while (pw >= p.Wg) { pw -= p.Wg; ++ph; }
+    while (ph >= p.Hg) { ph -= p.Hg; ++pt; }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_fwd_bf16_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + p.ctl_off);
+  float2* tab_s = reinterpret_cast<float2*>(smem + kOffTab);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  const int qblk = blockIdx.x % p.n_qblk;
+  const int bh = blockIdx.x / p.n_qblk;
+  const int b = bh / p.H;
+  const int h = bh - b * p.H;
+  const int q0 = qblk * kRowsPerCta;
+  const int nkv = (p.N + kBN - 1) / kBN;
+
+  const uint32_t sQ = smem_addr(smem + kOffQ);
+  const uint32_t sK = smem_addr(smem + kOffK);
+  const uint32_t sV = smem_addr(smem + kOffV);
+
+  if (tid == 0) {
+    for (int i = 0; i < kQTiles; ++i) {
+      mbar_init(smem_addr(&ctl->q_full[i]), 1);
+      mbar_init(smem_addr(&ctl->q_ready[i]), 128);
+      mbar_init(smem_addr(&ctl->s_full[i]), 1);
+      mbar_init(smem_addr(&ctl->p_ready[i]), 128);
+    }
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(smem_addr(&ctl->k_full[s]), 1);
+      mbar_init(smem_addr(&ctl->k_ready[s]), 128);
+      mbar_init(smem_addr(&ctl->k_empty[s]), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(smem_addr(&ctl->v_full[s]), 1);
+      mbar_init(smem_addr(&ctl->v_empty[s]), 1);
+    }
+    mbar_init(smem_addr(&ctl->o_final), 1);
+    ctl->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 13) {
+    tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (p.table_in_smem) {
+    for (int i = tid; i < p.table_entries; i += kThreads) tab_s[i] = p.table[i];
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctl->tmem_base;
+  volatile int* abort_flag = &ctl->abort_flag;
+
+  if (warp == 12) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      for (int i = 0; i < kQTiles; ++i) {
+        const uint32_t bar = smem_addr(&ctl->q_full[i]);
+        mbar_arrive_expect_tx(bar, kTileBytes);
+        const uint32_t dst = sQ + i * kTileBytes;
+        tma_load_4d(dst, &tm_q, bar, 0, h, q0 + i * kBM, b);
+        tma_load_4d(dst + kHalfBytes, &tm_q, bar, 64, h, q0 + i * kBM, b);
+      }
+      int k_issued = 0, v_issued = 0;
+      for (int j = 0; j < nkv; ++j) {
+        const int ks = j % kKStages, ku = j / kKStages;
+        if (ku > 0 && !mbar_wait(smem_addr(&ctl->k_empty[ks]), (ku - 1) & 1, abort_flag, kSiteKEmpty))
+          break;
+        {
+          const uint32_t bar = smem_addr(&ctl->k_full[ks]);
+          mbar_arrive_expect_tx(bar, kTileBytes);
+          const uint32_t dst = sK + ks * kTileBytes;
+          tma_load_4d(dst, &tm_k, bar, 0, h, j * kBN, b);
+          tma_load_4d(dst + kHalfBytes, &tm_k, bar, 64, h, j * kBN, b);
+          k_issued = j + 1;
+        }
+        const int vs = j % kVStages, vu = j / kVStages;
+        if (vu > 0 && !mbar_wait(smem_addr(&ctl->v_empty[vs]), (vu - 1) & 1, abort_flag, kSiteVEmpty))
+          break;
+        {
+          const uint32_t bar = smem_addr(&ctl->v_full[vs]);
+          mbar_arrive_expect_tx(bar, kTileBytes);
+          const uint32_t dst = sV + vs * kTileBytes;
+          tma_load_4d(dst, &tm_v, bar, 0, h, j * kBN, b);
+          tma_load_4d(dst + kHalfBytes, &tm_v, bar, 64, h, j * kBN, b);
+          v_issued = j + 1;
+        }
+      }
+      // Let every copy this thread started land before the CTA can retire.
+      for (int i = 0; i < kQTiles; ++i) drain_wait(smem_addr(&ctl->q_full[i]), 0);
+      for (int s = 0; s < kKStages; ++s) {
+        const int uses = k_issued > s ? (k_issued - 1 - s) / kKStages + 1 : 0;
+        if (uses > 0) drain_wait(smem_addr(&ctl->k_full[s]), (uses - 1) & 1);
+      }
+      for (int s = 0; s < kVStages; ++s) {
+        const int uses = v_issued > s ? (v_issued - 1 - s) / kVStages + 1 : 0;
+        if (uses > 0) drain_wait(smem_addr(&ctl->v_full[s]), (uses - 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 13) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdQK = idesc_bf16_f32(kBM, kBN, 0);
+      constexpr uint32_t kIdPV = idesc_bf16_f32(kBM, kD, 1);
+      const uint32_t tS0 = tmem + 0, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
+      bool ok = mbar_wait(smem_addr(&ctl->q_ready[0]), 0, abort_flag, kSiteQReady) &&
+                mbar_wait(smem_addr(&ctl->q_ready[1]), 0, abort_flag, kSiteQReady);
+      tc_fence_after_sync();
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int ks = j % kKStages;
+        if (!(ok = mbar_wait(smem_addr(&ctl->k_ready[ks]), (j / kKStages) & 1, abort_flag, kSiteKReady)))
+          break;
+        tc_fence_after_sync();
+        const uint32_t kt = sK + ks * kTileBytes;
+        issue_qk(tS0, sQ, kt, kIdQK);
+        mma_commit(smem_addr(&ctl->s_full[0]));
+        if (j > 0) {
+          if (!(ok = mbar_wait(smem_addr(&ctl->p_ready[1]), (j - 1) & 1, abort_flag, kSitePReady)))
+            break;
+          tc_fence_after_sync();
+          const int pvs = (j - 1) % kVStages;
+          issue_pv(tO1, tS1, sV + pvs * kTileBytes, kIdPV, j - 1 > 0);
+          mma_commit(smem_addr(&ctl->v_empty[pvs]));
+        }
+        issue_qk(tS1, sQ + kTileBytes, kt, kIdQK);
+        mma_commit(smem_addr(&ctl->s_full[1]));
+        mma_commit(smem_addr(&ctl->k_empty[ks]));
+        const int vs = j % kVStages;
+        if (!(ok = mbar_wait(smem_addr(&ctl->v_full[vs]), (j / kVStages) & 1, abort_flag, kSiteVFull)))
+          break;
+        if (!(ok = mbar_wait(smem_addr(&ctl->p_ready[0]), j & 1, abort_flag, kSitePReady))) break;
+        tc_fence_after_sync();
+        issue_pv(tO0, tS0, sV + vs * kTileBytes, kIdPV, j > 0);
+      }
+      if (ok) {
+        const int jl = nkv - 1;
+        if (mbar_wait(smem_addr(&ctl->p_ready[1]), jl & 1, abort_flag, kSitePReady)) {
+          tc_fence_after_sync();
+          issue_pv(tO1, tS1, sV + (jl % kVStages) * kTileBytes, kIdPV, jl > 0);
+        }
+      }
+      mma_commit(smem_addr(&ctl->o_final));
+      drain_wait(smem_addr(&ctl->o_final), 0);
+    }
+    __syncwarp();
+  } else if (warp >= 8 && warp < 12) {
+    // ------------------------------------------------------------ RoPE on Q and K tiles
+    const float2* tab = p.table_in_smem ? tab_s : p.table;
+    const RopeLane L = make_rope_lane(p, tid - 256);
+    bool ok = true;
+    for (int i = 0; i < kQTiles && ok; ++i) {
+      if (!(ok = mbar_wait(smem_addr(&ctl->q_full[i]), 0, abort_flag, kSiteQFull))) break;
+      rope_tile(p, L, smem + kOffQ + i * kTileBytes, q0 + i * kBM, tab);
+      fence_proxy_async_smem();
+      mbar_arrive(smem_addr(&ctl->q_ready[i]));
+    }
+    for (int j = 0; ok && j < nkv; ++j) {
+      const int ks = j % kKStages;
+      if (!(ok = mbar_wait(smem_addr(&ctl->k_full[ks]), (j / kKStages) & 1, abort_flag, kSiteKFull)))
+        break;
+      rope_tile(p, L, smem + kOffK + ks * kTileBytes, j * kBN, tab);
+      fence_proxy_async_smem();
+      mbar_arrive(smem_addr(&ctl->k_ready[ks]));
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int qi = warp >> 2;
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_bits = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_bits + 128 * qi;
+    const uint32_t tO = tmem + lane_bits + 256 + 128 * qi;
+    const float c = p.scale_log2;
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    bool ok = true;
+    uint32_t r[32];
+    for (int j = 0; j < nkv; ++j) {
+      if (!(ok = mbar_wait(smem_addr(&ctl->s_full[qi]), j & 1, abort_flag, kSiteSFull))) break;
+      tc_fence_after_sync();
+      const int valid = min(kBN, p.N - j * kBN);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        tmem_ld32(tS + ch * 32, r);
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (ch * 32 + e < valid) mx = fmaxf(mx, __uint_as_float(r[e]));
+      }
+      const float m_new = fmaxf(m_run, mx * c);
+      const bool resc = m_new > m_run + 8.0f;
+      float alpha = 1.f;
+      if (resc) {
+        alpha = ex2_approx(m_run - m_new);
+        l_run *= alpha;
+        m_run = m_new;
+      }
+      float lsum = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        tmem_ld32(tS + ch * 32, r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e2 = 0; e2 < 16; ++e2) {
+          const int e = 2 * e2;
+          const float p0 = (ch * 32 + e < valid) ? ex2_approx(fmaf(__uint_as_float(r[e]), c, -m_run)) : 0.f;
+          const float p1 = (ch * 32 + e + 1 < valid) ? ex2_approx(fmaf(__uint_as_float(r[e + 1]), c, -m_run)) : 0.f;
+          lsum += p0 + p1;
+          pk[e2] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + ch * 16, pk);
+      }
+      l_run += lsum;
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          tmem_ld32(tO + ch * 32, r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          tmem_st32(tO + ch * 32, r);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(smem_addr(&ctl->p_ready[qi]));
+    }
+    if (ok) ok = mbar_wait(smem_addr(&ctl->o_final), 0, abort_flag, kSiteOFinal);
+    if (ok) {
+      tc_fence_after_sync();
+      const int n = q0 + qi * kBM + row;
+      const bool live = n < p.N;
+      const float inv_l = 1.f / l_run;
+      __nv_bfloat16* orow = p.out + ((static_cast<size_t>(b) * p.N + (live ? n : 0)) * p.H + h) * kD;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        tmem_ld32(tO + ch * 32, r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e2 = 0; e2 < 16; ++e2)
+          pk[e2] = pack_bf16x2(__uint_as_float(r[2 * e2]) * inv_l, __uint_as_float(r[2 * e2 + 1]) * inv_l);
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      if (live && p.lse != nullptr)
+        p.lse[(static_cast<size_t>(b) * p.H + h) * p.N + n] = (m_run + __log2f(l_run)) * 0.69314718055994530942f;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 13) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t read_and_clear_error_word_sm103(unsigned int* word) {
+  cudaError_t e = cudaMemcpyFromSymbol(word, g_error_word, sizeof(unsigned int));
+  if (e != cudaSuccess || *word == 0) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+}
+
+cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, cudaStream_t stream,
+                                   const char** what) {
+  *what = nullptr;
+  CUtensorMap maps[3];
+  const void* srcs[3] = {pr.q, pr.k, pr.v};
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(pr.H),
+                              static_cast<cuuint64_t>(pr.N), static_cast<cuuint64_t>(pr.B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kD) * 2,
+                                 static_cast<cuuint64_t>(pr.H) * kD * 2,
+                                 static_cast<cuuint64_t>(pr.N) * pr.H * kD * 2};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBN), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  for (int i = 0; i < 3; ++i) {
+    CUresult r = encode(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(srcs[i]),
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      *what = "cuTensorMapEncodeTiled failed";
+      return cudaErrorInvalidValue;
+    }
+  }
+  Params p{};
+  p.B = pr.B; p.H = pr.H; p.N = pr.N; p.Hg = pr.Hg; p.Wg = pr.Wg; p.HgWg = pr.Hg * pr.Wg;
+  p.half_t = pr.half_t; p.half_h = pr.half_h; p.half_w = pr.half_w;
+  p.off_h = pr.T * pr.half_t;
+  p.off_w = p.off_h + pr.Hg * pr.half_h;
+  p.table_entries = pr.table_entries;
+  p.n_qblk = (pr.N + kRowsPerCta - 1) / kRowsPerCta;
+  p.scale_log2 = pr.scale * 1.4426950408889634f;
+  p.table = pr.table;
+  p.out = static_cast<__nv_bfloat16*>(pr.out);
+  p.lse = pr.lse;
+  const int tab_bytes = ((pr.table_entries * 8) + 15) & ~15;
+  const int ctl_bytes = (static_cast<int>(sizeof(Ctl)) + 15) & ~15;
+  int smem = kOffTab + tab_bytes + ctl_bytes + 1024;
+  if (smem <= kMaxDynSmem) {
+    p.table_in_smem = 1;
+    p.ctl_off = kOffTab + tab_bytes;
+  } else {
+    p.table_in_smem = 0;
+    p.ctl_off = kOffTab;
+    smem = kOffTab + ctl_bytes + 1024;
+  }
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_sm103, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) {
+    *what = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+    return e;
+  }
+  const long long grid = static_cast<long long>(pr.B) * pr.H * p.n_qblk;
+  if (grid > 0x7fffffffLL) {
+    *what = "grid too large";
+    return cudaErrorInvalidValue;
+  }
+  attn_fwd_bf16_sm103<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(maps[0], maps[1], maps[2], p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) *what = "kernel launch failed";
+  return e;
+}
+
+}  // namespace vdx

@@ -1,0 +1,226 @@
+// C-ABI front end: argument checks, the per-device cos/sin table cache, the device error
+// word, and dispatch to the bf16 tensor-core kernel or the fp32 CUDA-core kernel.
+//
+// The cos/sin table realises the rotary angles of vidax: A Unified JAX Framework for Video
+// Generative Models on Accelerator Meshes, §2 "3D RoPE, 3D VAEs, and flash attention": for
+// axis a with S_a rotary dims and pair j < S_a/2, angle = pos * theta^(-2j/S_a), evaluated in
+// double precision and stored as float (cos, sin).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "vdx.h"
+#include "vdx_internal.h"
+
+namespace {
+
+thread_local std::string t_last_error;
+
+vdx_status fail(vdx_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return s;
+}
+
+using TableKey = std::tuple<int, int, int, int, int, int, int, double>;   // dev,T,Hg,Wg,st,sh,sw,theta
+struct TableEntry {
+  float2* ptr;
+  int entries;
+};
+std::mutex g_mu;
+std::map<TableKey, TableEntry> g_tables;
+vdx::EncodeTiledFn g_encode = nullptr;
+
+// Entries: [T][st/2] then [Hg][sh/2] then [Wg][sw/2], each (cos, sin) of pos * theta^(-2j/S).
+std::vector<float2> build_table(int T, int Hg, int Wg, int st, int sh, int sw, double theta) {
+  std::vector<float2> tab;
+  const int extents[3] = {T, Hg, Wg};
+  const int secs[3] = {st, sh, sw};
+  for (int a = 0; a < 3; ++a) {
+    const int half = secs[a] / 2;
+    for (int pos = 0; pos < extents[a]; ++pos) {
+      for (int j = 0; j < half; ++j) {
+        const double omega = std::pow(theta, -2.0 * j / secs[a]);
+        const double ang = static_cast<double>(pos) * omega;
+        tab.push_back(make_float2(static_cast<float>(std::cos(ang)), static_cast<float>(std::sin(ang))));
+      }
+    }
+  }
+  return tab;
+}
+
+vdx_status get_table(int T, int Hg, int Wg, int st, int sh, int sw, double theta,
+                     const float2** out, int* entries) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(VDX_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  const TableKey key{dev, T, Hg, Wg, st, sh, sw, theta};
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = g_tables.find(key);
+  if (it == g_tables.end()) {
+    std::vector<float2> host = build_table(T, Hg, Wg, st, sh, sw, theta);
+    float2* d = nullptr;
+    const size_t bytes = std::max<size_t>(host.size(), 1) * sizeof(float2);
+    e = cudaMalloc(&d, bytes);
+    if (e != cudaSuccess) return fail(VDX_ERR_CUDA, "cudaMalloc(table): %s", cudaGetErrorString(e));
+    if (!host.empty()) {
+      e = cudaMemcpy(d, host.data(), host.size() * sizeof(float2), cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) {
+        cudaFree(d);
+        return fail(VDX_ERR_CUDA, "cudaMemcpy(table): %s", cudaGetErrorString(e));
+      }
+    }
+    it = g_tables.emplace(key, TableEntry{d, static_cast<int>(host.size())}).first;
+  }
+  *out = it->second.ptr;
+  *entries = it->second.entries;
+  return VDX_OK;
+}
+
+vdx_status get_encode(vdx::EncodeTiledFn* fn) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_encode == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || p == nullptr)
+      return fail(VDX_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(e));
+    g_encode = reinterpret_cast<vdx::EncodeTiledFn>(p);
+  }
+  *fn = g_encode;
+  return VDX_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// Shared argument checks; fills `p` (except the table) on success.
+vdx_status prepare(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                   int H, int T, int Hg, int Wg, int d, int st, int sh, int sw, double theta,
+                   float scale, size_t esize, vdx::Problem* p) {
+  if (!q || !k || !v || !out) return fail(VDX_ERR_ARG, "q, k, v and out must be non-NULL");
+  if (B < 1 || H < 1 || T < 1 || Hg < 1 || Wg < 1 || d < 2)
+    return fail(VDX_ERR_ARG, "B, H, T, Hgrid, Wgrid must be >= 1 and d >= 2 (got %d %d %d %d %d, d=%d)",
+                B, H, T, Hg, Wg, d);
+  if (st == 0 && sh == 0 && sw == 0) {
+    sh = sw = 2 * (d / 6);
+    st = d - sh - sw;
+  }
+  if (st < 0 || sh < 0 || sw < 0 || (st | sh | sw) & 1 || st + sh + sw != d)
+    return fail(VDX_ERR_ARG, "rotary sections %d/%d/%d must be even, non-negative and sum to d=%d",
+                st, sh, sw, d);
+  if (!(theta > 0.0) || !std::isfinite(theta)) return fail(VDX_ERR_ARG, "theta must be > 0");
+  if (!std::isfinite(scale)) return fail(VDX_ERR_ARG, "scale must be finite");
+  const long long N = static_cast<long long>(T) * Hg * Wg;
+  if (N > 0x7fffffffLL / 2) return fail(VDX_ERR_ARG, "N = T*Hgrid*Wgrid = %lld is too large", N);
+  const long long elems = static_cast<long long>(B) * N * H * d;
+  if (elems > (1LL << 46)) return fail(VDX_ERR_ARG, "tensor too large");
+  const void* ptrs[5] = {q, k, v, out, lse};
+  for (int i = 0; i < 5; ++i)
+    if (ptrs[i] && (reinterpret_cast<uintptr_t>(ptrs[i]) & 15))
+      return fail(VDX_ERR_ALIGN, "pointer argument %d is not 16-byte aligned", i);
+  const size_t bytes = static_cast<size_t>(elems) * esize;
+  if (overlaps(out, bytes, q, bytes) || overlaps(out, bytes, k, bytes) || overlaps(out, bytes, v, bytes))
+    return fail(VDX_ERR_ARG, "out overlaps q, k or v");
+  if (lse) {
+    const size_t lb = static_cast<size_t>(B) * H * N * sizeof(float);
+    if (overlaps(lse, lb, out, bytes) || overlaps(lse, lb, q, bytes) || overlaps(lse, lb, k, bytes) ||
+        overlaps(lse, lb, v, bytes))
+      return fail(VDX_ERR_ARG, "lse overlaps q, k, v or out");
+  }
+  p->q = q; p->k = k; p->v = v; p->out = out; p->lse = lse;
+  p->B = B; p->H = H; p->T = T; p->Hg = Hg; p->Wg = Wg; p->N = static_cast<int>(N); p->d = d;
+  p->half_t = st / 2; p->half_h = sh / 2; p->half_w = sw / 2;
+  p->scale = scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  const float2* tab = nullptr;
+  int entries = 0;
+  vdx_status s = get_table(T, Hg, Wg, st, sh, sw, theta, &tab, &entries);
+  if (s != VDX_OK) return s;
+  p->table = tab;
+  p->table_entries = entries;
+  return VDX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+vdx_status vdx_rope3d_attn(const void* q, const void* k, const void* v, void* out, float* lse,
+                           int B, int H, int T, int Hgrid, int Wgrid, int d, int sec_t, int sec_h,
+                           int sec_w, double theta, float scale, void* stream) {
+  t_last_error.clear();
+  if (d != 128) return fail(VDX_ERR_UNSUPPORTED, "bf16 path supports head_dim 128 only (got %d)", d);
+  vdx::Problem p{};
+  vdx_status s = prepare(q, k, v, out, lse, B, H, T, Hgrid, Wgrid, d, sec_t, sec_h, sec_w, theta,
+                         scale, 2, &p);
+  if (s != VDX_OK) return s;
+  vdx::EncodeTiledFn enc = nullptr;
+  if ((s = get_encode(&enc)) != VDX_OK) return s;
+  const char* what = nullptr;
+  cudaError_t e = vdx::launch_attn_bf16_sm103(p, enc, static_cast<cudaStream_t>(stream), &what);
+  if (e != cudaSuccess)
+    return fail(VDX_ERR_CUDA, "%s: %s", what ? what : "launch", cudaGetErrorString(e));
+  return VDX_OK;
+}
+
+vdx_status vdx_rope3d_attn_f32(const float* q, const float* k, const float* v, float* out,
+                               float* lse, int B, int H, int T, int Hgrid, int Wgrid, int d,
+                               int sec_t, int sec_h, int sec_w, double theta, float scale,
+                               void* stream) {
+  t_last_error.clear();
+  if (d != 64 && d != 128)
+    return fail(VDX_ERR_UNSUPPORTED, "fp32 path supports head_dim 64 or 128 (got %d)", d);
+  vdx::Problem p{};
+  vdx_status s = prepare(q, k, v, out, lse, B, H, T, Hgrid, Wgrid, d, sec_t, sec_h, sec_w, theta,
+                         scale, 4, &p);
+  if (s != VDX_OK) return s;
+  cudaError_t e = vdx::launch_attn_f32(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(VDX_ERR_CUDA, "fp32 kernel launch: %s", cudaGetErrorString(e));
+  return VDX_OK;
+}
+
+vdx_status vdx_sync_check(void* stream) {
+  t_last_error.clear();
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(VDX_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+  unsigned int word = 0;
+  e = vdx::read_and_clear_error_word_sm103(&word);
+  if (e != cudaSuccess) return fail(VDX_ERR_CUDA, "reading the error word: %s", cudaGetErrorString(e));
+  if (word != 0)
+    return fail(VDX_ERR_TIMEOUT, "a kernel pipeline wait gave up (site %u)", (word >> 8) & 0xff);
+  return VDX_OK;
+}
+
+const char* vdx_last_error(void) { return t_last_error.c_str(); }
+
+void vdx_shutdown(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto& kv : g_tables) {
+    cudaSetDevice(std::get<0>(kv.first));
+    cudaFree(kv.second.ptr);
+  }
+  cudaSetDevice(cur);
+  g_tables.clear();
+}
+
+int vdx_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,41 @@
+// Internal interface between the C-ABI front end (vdx_capi.cu) and the kernel translation
+// units.  Not part of the public API.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <vector_types.h>
+#include <cstdint>
+
+namespace vdx {
+
+// One attention problem, already validated, with its cos/sin table resident on the device.
+// The table holds float2 (cos, sin) entries in three consecutive blocks:
+//   [T][sec_t/2], then [Hgrid][sec_h/2], then [Wgrid][sec_w/2].
+struct Problem {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  float* lse;           // may be nullptr
+  int B, H, T, Hg, Wg, N, d;
+  int half_t, half_h, half_w;   // rotary pairs per axis
+  float scale;
+  const float2* table;
+  int table_entries;
+};
+
+// bf16, d = 128, tcgen05 kernel (attn_fwd_sm103.cu).  `encode` is cuTensorMapEncodeTiled.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+cudaError_t launch_attn_bf16_sm103(const Problem& p, EncodeTiledFn encode, cudaStream_t stream,
+                                   const char** what);
+
+// Read the tensor-core kernel's device error word (synchronous) and reset it to 0.
+cudaError_t read_and_clear_error_word_sm103(unsigned int* word);
+
+// fp32, d in {64, 128}, CUDA-core kernel (attn_fwd_f32.cu).
+cudaError_t launch_attn_f32(const Problem& p, cudaStream_t stream);
+
+}  // namespace vdx
