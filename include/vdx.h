@@ -43,10 +43,14 @@ typedef enum {
   VDX_ERR_ALIGN = 2,        /* a pointer is not 16-byte aligned                       */
   VDX_ERR_UNSUPPORTED = 3,  /* valid, but outside what this build implements          */
   VDX_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed                      */
-  VDX_ERR_TIMEOUT = 5       /* a kernel pipeline wait gave up (see vdx_sync_check)    */
+  VDX_ERR_TIMEOUT = 5,      /* a kernel pipeline wait gave up (see vdx_sync_check)    */
+  VDX_ERR_RANGE = 6         /* a rotated q/k value left the fp16 operand range         */
 } vdx_status;
 
 /* bf16 path, tcgen05 tensor cores.  q, k, v, out: __nv_bfloat16 [B, N, H, d]; d must be 128.
+ * Arithmetic: rotation in fp32; rotated q and k rounded to fp16 for QK^T (so |q|, |k| must stay
+ * below ~46000, else values are clamped and vdx_sync_check reports VDX_ERR_RANGE); scores,
+ * softmax statistics and the output accumulator in fp32; P and v enter PV as bf16.
  * sec_t/sec_h/sec_w: even, sum to d; all three 0 selects d - 4*(d/6), 2*(d/6), 2*(d/6)
  * (44/42/42 at d = 128).  scale <= 0 selects 1/sqrt(d).  theta > 0 (10000 for Wan).
  * out must not overlap q, k or v.  B, H, T, Hgrid, Wgrid >= 1. */
@@ -64,7 +68,8 @@ vdx_status vdx_rope3d_attn_f32(const float* q, const float* k, const float* v, f
 
 /* Synchronise `stream`, then read and clear the device error word.  Returns VDX_OK,
  * VDX_ERR_TIMEOUT (a kernel gave up on a pipeline wait; the output of that call is
- * undefined) or VDX_ERR_CUDA (an asynchronous CUDA error is pending). */
+ * undefined), VDX_ERR_RANGE (a rotated q/k value was clamped to the fp16 range; the output
+ * is inexact) or VDX_ERR_CUDA (an asynchronous CUDA error is pending). */
 vdx_status vdx_sync_check(void* stream);
 
 /* Message for the last non-OK status returned on this host thread ("" if none). */

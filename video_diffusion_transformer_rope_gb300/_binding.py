@@ -8,9 +8,10 @@ import os
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libvdx.so")
 
-VDX_OK, VDX_ERR_ARG, VDX_ERR_ALIGN, VDX_ERR_UNSUPPORTED, VDX_ERR_CUDA, VDX_ERR_TIMEOUT = range(6)
+(VDX_OK, VDX_ERR_ARG, VDX_ERR_ALIGN, VDX_ERR_UNSUPPORTED, VDX_ERR_CUDA, VDX_ERR_TIMEOUT,
+ VDX_ERR_RANGE) = range(7)
 STATUS_NAMES = {0: "VDX_OK", 1: "VDX_ERR_ARG", 2: "VDX_ERR_ALIGN", 3: "VDX_ERR_UNSUPPORTED",
-                4: "VDX_ERR_CUDA", 5: "VDX_ERR_TIMEOUT"}
+                4: "VDX_ERR_CUDA", 5: "VDX_ERR_TIMEOUT", 6: "VDX_ERR_RANGE"}
 
 _p, _i, _d, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_float
 # name -> (restype, argtypes); mirrors include/vdx.h

@@ -3,7 +3,9 @@
 // Operation: vidax: A Unified JAX Framework for Video Generative Models on Accelerator
 // Meshes, §2 "3D RoPE, 3D VAEs, and flash attention" (rotary 3D positions on Q and K, then
 // attention without materialising the N x N scores).  bf16 in/out, d = 128, fp32 softmax
-// statistics and accumulators.
+// statistics and accumulators.  The rotated Q and K are rounded to fp16 (11-bit significand,
+// 8x finer than bf16) for the QK^T product, whose error then stays well inside the lse
+// tolerance for ordinary activations; P and V enter the PV product as bf16.
 //
 // One CTA owns 256 query rows (two 128-row Q tiles) of one (batch, head) and streams every
 // 128-key K/V tile of that head:
@@ -11,6 +13,7 @@
 //   warps 0-3   softmax for Q tile 0   (thread = one query row = one TMEM lane)
 //   warps 4-7   softmax for Q tile 1
 //   warps 8-11  RoPE: rotate Q tiles once, and each K tile in shared memory as it lands
+//               (bf16 in, fp16 out, in place)
 //   warp  12    TMA producer: Q tiles once, then K/V tiles into two 2-stage rings
 //   warp  13    tcgen05 MMA issuer (one thread) and TMEM owner
 //   warps 14-15 idle
@@ -96,6 +99,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Round to fp16 with saturation to +-65504 (no infinities); `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // Bounded wait used on the way out: ignores the abort flag so that copies / MMAs that are
 // still in flight finish before shared or tensor memory is released.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -167,10 +177,12 @@ __device__ __forceinline__ RopeLane make_rope_lane(const Params& p, int t) {
   return L;
 }
 
-__device__ __forceinline__ void rope_tile(const Params& p, const RopeLane& L, uint8_t* tile,
-                                          int n_first, const float2* __restrict__ tab) {
+// Rotates bf16 in place into fp16; returns the largest |rotated value| seen.
+__device__ __forceinline__ float rope_tile(const Params& p, const RopeLane& L, uint8_t* tile,
+                                           int n_first, const float2* __restrict__ tab) {
+  float amax = 0.f;
   int n = n_first + L.rsub;
-  if (n >= p.N) return;
+  if (n >= p.N) return amax;
   int pt = n / p.HgWg;
   int rem = n - pt * p.HgWg;
   int ph = rem / p.Wg;
@@ -189,7 +201,8 @@ __device__ __forceinline__ void rope_tile(const Params& p, const RopeLane& L, ui
       const float x0 = __low2float(v2), x1 = __high2float(v2);
       const float y0 = fmaf(x0, cs.x, -x1 * cs.y);
       const float y1 = fmaf(x0, cs.y, x1 * cs.x);
-      w[e] = pack_bf16x2(y0, y1);
+      amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
+      w[e] = pack_f16x2_sat(y0, y1);
     }
     *ptr = make_uint4(w[0], w[1], w[2], w[3]);
     n += 8;
@@ -197,6 +210,7 @@ __device__ __forceinline__ void rope_tile(const Params& p, const RopeLane& L, ui
     while (pw >= p.Wg) { pw -= p.Wg; ++ph; }
     while (ph >= p.Hg) { ph -= p.Hg; ++pt; }
   }
+  return amax;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -309,8 +323,8 @@ attn_fwd_bf16_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdQK = idesc_bf16_f32(kBM, kBN, 0);
-      constexpr uint32_t kIdPV = idesc_bf16_f32(kBM, kD, 1);
+      constexpr uint32_t kIdQK = idesc_f16kind_f32acc(kBM, kBN, 0, 0);   // fp16 Q', K'
+      constexpr uint32_t kIdPV = idesc_f16kind_f32acc(kBM, kD, 1, 1);   // bf16 P, V (MN-major)
       const uint32_t tS0 = tmem + 0, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
       bool ok = mbar_wait(smem_addr(&ctl->q_ready[0]), 0, abort_flag, kSiteQReady) &&
                 mbar_wait(smem_addr(&ctl->q_ready[1]), 0, abort_flag, kSiteQReady);
@@ -357,9 +371,10 @@ attn_fwd_bf16_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const float2* tab = p.table_in_smem ? tab_s : p.table;
     const RopeLane L = make_rope_lane(p, tid - 256);
     bool ok = true;
+    float amax = 0.f;
     for (int i = 0; i < kQTiles && ok; ++i) {
       if (!(ok = mbar_wait(smem_addr(&ctl->q_full[i]), 0, abort_flag, kSiteQFull))) break;
-      rope_tile(p, L, smem + kOffQ + i * kTileBytes, q0 + i * kBM, tab);
+      amax = fmaxf(amax, rope_tile(p, L, smem + kOffQ + i * kTileBytes, q0 + i * kBM, tab));
       fence_proxy_async_smem();
       mbar_arrive(smem_addr(&ctl->q_ready[i]));
     }
@@ -367,10 +382,11 @@ attn_fwd_bf16_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const int ks = j % kKStages;
       if (!(ok = mbar_wait(smem_addr(&ctl->k_full[ks]), (j / kKStages) & 1, abort_flag, kSiteKFull)))
         break;
-      rope_tile(p, L, smem + kOffK + ks * kTileBytes, j * kBN, tab);
+      amax = fmaxf(amax, rope_tile(p, L, smem + kOffK + ks * kTileBytes, j * kBN, tab));
       fence_proxy_async_smem();
       mbar_arrive(smem_addr(&ctl->k_ready[ks]));
     }
+    if (!(amax <= 65504.f)) atomicOr(&g_error_word, 2u);
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax + epilogue
     const int qi = warp >> 2;

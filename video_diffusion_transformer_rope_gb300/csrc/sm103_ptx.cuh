@@ -10,6 +10,7 @@ namespace vdx {
 
 // Device error word of the translation unit that includes this header (one per TU: device
 // code is compiled without relocatable linking).  Bit 0 = a bounded wait timed out,
+// bit 1 = a rotated q/k value exceeded the fp16 operand range (it was clamped),
 // bits 8..15 = the wait site that gave up first.
 __device__ unsigned int g_error_word = 0;
 
@@ -185,11 +186,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor for kind::f16: fp32 accumulator, bf16 A and B, M x N tile,
-// A K-major, B K-major (b_mn_major = 0) or MN-major (1).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn_major) << 16) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+// Instruction descriptor for kind::f16 with an fp32 accumulator and an M x N tile.
+// ab_type: 0 = fp16 A and B, 1 = bf16 A and B (the two operands always share one type).
+// A is K-major; B is K-major (b_mn_major = 0) or MN-major (1).
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32acc(int M, int N, uint32_t ab_type,
+                                                            int b_mn_major) {
+  return (1u << 4) | (ab_type << 7) | (ab_type << 10) |
+         (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

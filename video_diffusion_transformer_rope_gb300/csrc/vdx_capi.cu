@@ -202,8 +202,11 @@ vdx_status vdx_sync_check(void* stream) {
   unsigned int word = 0;
   e = vdx::read_and_clear_error_word_sm103(&word);
   if (e != cudaSuccess) return fail(VDX_ERR_CUDA, "reading the error word: %s", cudaGetErrorString(e));
-  if (word != 0)
+  if (word & 1u)
     return fail(VDX_ERR_TIMEOUT, "a kernel pipeline wait gave up (site %u)", (word >> 8) & 0xff);
+  if (word & 2u)
+    return fail(VDX_ERR_RANGE, "a rotated q/k value exceeded the fp16 operand range (|x| > 65504); "
+                               "it was clamped and the result is inexact");
   return VDX_OK;
 }
 
