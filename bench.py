@@ -282,7 +282,7 @@ def run_ours(args, w):
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         hq64, hk64, hv64 = hq, hk, hv
-        heads, rph = 4, 64
+        heads, rph = 16, 256
         dt, rows = _cpu_oracle_sample(w, hq64, hk64, hv64, heads, rph)
         cpu_tf = 4.0 * w.N * w.d * rows / dt / 1e12
         cpu = {"value": cpu_tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
