@@ -183,8 +183,8 @@ def run_reference(args, w):
     return 0
 
 
-def _config(w):
-    return {"workload": w.name, "B": w.B, "heads": w.H, "head_dim": w.d,
+def _config(w, k_rope="prepass"):
+    return {"workload": w.name, "k_rope": k_rope, "B": w.B, "heads": w.H, "head_dim": w.d,
             "grid": f"{w.T}x{w.Hg}x{w.Wg}", "N": w.N,
             "sections": "/".join(map(str, w.sections)), "theta": w.theta,
             "l2": "inputs larger than L2 (q, k, v 1.55 GB each); no flush",
@@ -216,8 +216,13 @@ def run_ours(args, w):
     grid = (w.T, w.Hg, w.Wg)
     stream = torch.cuda.current_stream()
 
+    k_mode = {"prepass": vdx.K_ROPE_PREPASS, "fused": vdx.K_ROPE_FUSED}[args.k_rope]
+    k_ws = torch.empty(vdx.workspace_bytes(w.B, w.H, grid, w.d) // 2, dtype=torch.float16,
+                       device=dev) if args.k_rope == "prepass" else None
+
     def step():
-        vdx.rope3d_attn(q, k, v, grid, w.sections, w.theta, out=out, lse=lse, stream=stream)
+        vdx.rope3d_attn(q, k, v, grid, w.sections, w.theta, out=out, lse=lse, stream=stream,
+                        k_rope=k_mode, workspace=k_ws)
 
     for _ in range(args.warmup):
         step()
@@ -295,15 +300,16 @@ def run_ours(args, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) on device, bf16)",
-            "config": _config(w),
+            "config": _config(w, args.k_rope),
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if args.k_rope == "prepass" else 1),
             "roofline": {"bound": "tensor", "achieved": tflops_rank, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops_rank / peak, "traffic": traffic,
                          "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)",
                          "frac_of_sustained": (tflops_rank / peak_sus) if peak_sus else None,
-                         "kernel": "attn_fwd_bf16_sm103"},
+                         "kernel": "attn_fwd_sm103 (+ rope3d_k_prepass)" if args.k_rope == "prepass"
+                         else "attn_fwd_sm103 (fused K rotation)"},
             "cpu_baseline": cpu,
             "clocks": clocks,
         }
@@ -321,6 +327,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=configs.WAN14B_720P.name, choices=sorted(configs.BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--k-rope", choices=["prepass", "fused"], default="prepass",
+                    help="K rotated once by a prepass kernel (default) or per tile inside the "
+                         "attention kernel")
     args = ap.parse_args()
     w = configs.BY_NAME[args.workload]
     if args.impl == "reference":

@@ -33,6 +33,8 @@
 #ifndef VDX_H_
 #define VDX_H_
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -47,6 +49,23 @@ typedef enum {
   VDX_ERR_RANGE = 6         /* a rotated q/k value left the fp16 operand range         */
 } vdx_status;
 
+/* How K gets rotated on the bf16 path. */
+#define VDX_K_ROPE_DEFAULT 0  /* = VDX_K_ROPE_PREPASS                                          */
+#define VDX_K_ROPE_PREPASS 1  /* a prepass kernel rotates every key token once into an fp16
+                                 workspace [B, N, H, d]; the attention kernel streams it      */
+#define VDX_K_ROPE_FUSED 2    /* each CTA rotates every K tile in shared memory as it lands
+                                 (no workspace; the rotation is repeated per query block)     */
+
+typedef struct vdx_attn_options {
+  int k_rope;               /* one of VDX_K_ROPE_*                                              */
+  void* workspace;          /* device scratch for the prepass, >= vdx_rope3d_workspace_bytes()
+                               bytes, 16-byte aligned, not overlapping q/k/v/out; NULL = a
+                               library-owned per-device buffer (allocated or grown with
+                               cudaMalloc on first need; shared by every call on that device, so
+                               calls that may overlap on different streams should pass their own) */
+  size_t workspace_bytes;   /* size of `workspace` in bytes                                      */
+} vdx_attn_options;
+
 /* bf16 path, tcgen05 tensor cores.  q, k, v, out: __nv_bfloat16 [B, N, H, d]; d must be 128.
  * Arithmetic: rotation in fp32; rotated q and k rounded to fp16 for QK^T (so |q|, |k| must stay
  * below ~46000, else values are clamped and vdx_sync_check reports VDX_ERR_RANGE); scores,
@@ -58,6 +77,16 @@ vdx_status vdx_rope3d_attn(const void* q, const void* k, const void* v, void* ou
                            int B, int H, int T, int Hgrid, int Wgrid, int d,
                            int sec_t, int sec_h, int sec_w, double theta, float scale,
                            void* stream);
+
+/* Same as vdx_rope3d_attn with explicit options (NULL = defaults: K prepass, library-owned
+ * workspace). */
+vdx_status vdx_rope3d_attn_ex(const void* q, const void* k, const void* v, void* out, float* lse,
+                              int B, int H, int T, int Hgrid, int Wgrid, int d,
+                              int sec_t, int sec_h, int sec_w, double theta, float scale,
+                              const vdx_attn_options* opt, void* stream);
+
+/* Bytes of workspace the K prepass needs for this problem (B*N*H*d*2), 0 for invalid sizes. */
+size_t vdx_rope3d_workspace_bytes(int B, int H, int T, int Hgrid, int Wgrid, int d);
 
 /* fp32 path (CUDA cores, fp32 arithmetic throughout).  Same operation and rules; q, k, v,
  * out are float [B, N, H, d]; d must be 64 or 128. */

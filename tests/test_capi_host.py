@@ -21,15 +21,13 @@ def L():
 def _declared():
     hdr = open(os.path.join(ROOT, "include", "vdx.h")).read()
     hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
-    return set(re.findall(r"^\s*(?:vdx_status|const char\s*\*|void|int)\s+(vdx_\w+)\s*\(", hdr, re.M))
+    return set(re.findall(r"^\s*(?:vdx_status|const char\s*\*|void|int|size_t)\s+(vdx_\w+)\s*\(", hdr, re.M))
 
 
 def test_exports_every_declared_symbol(L):
     decl = _declared()
-    assert decl == {"vdx_rope3d_attn", "vdx_rope3d_attn_f32", "vdx_sync_check", "vdx_last_error",
-                    "vdx_shutdown", "vdx_version"} | (decl - {"vdx_rope3d_attn", "vdx_rope3d_attn_f32",
-                                                              "vdx_sync_check", "vdx_last_error",
-                                                              "vdx_shutdown", "vdx_version"})
+    assert {"vdx_rope3d_attn", "vdx_rope3d_attn_ex", "vdx_rope3d_attn_f32", "vdx_sync_check",
+            "vdx_last_error", "vdx_shutdown", "vdx_version", "vdx_rope3d_workspace_bytes"} <= decl
     for name in decl:
         assert hasattr(L, name), name
     assert set(_binding.SIGNATURES) == decl
@@ -69,6 +67,19 @@ def _call(L, fn="vdx_rope3d_attn", q=FAKE, k=FAKE + (1 << 32), v=FAKE + (2 << 32
 def test_rejects_bad_arguments_without_cuda(L, kw, status, msg):
     assert _call(L, **kw) == status
     assert msg in L.vdx_last_error().decode()
+
+
+def test_workspace_bytes(L):
+    assert L.vdx_rope3d_workspace_bytes(2, 40, 21, 45, 80, 128) == 2 * 75600 * 40 * 128 * 2
+    assert L.vdx_rope3d_workspace_bytes(0, 40, 21, 45, 80, 128) == 0
+
+
+def test_ex_rejects_bad_options(L):
+    opt = _binding.AttnOptions(7, None, 0)
+    r = L.vdx_rope3d_attn_ex(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + (1 << 32)),
+                             ctypes.c_void_p(FAKE + (2 << 32)), ctypes.c_void_p(FAKE + (3 << 32)),
+                             None, 1, 2, 2, 3, 4, 128, 0, 0, 0, 10000.0, 0.0, ctypes.byref(opt), None)
+    assert r == _binding.VDX_ERR_ARG and "k_rope" in L.vdx_last_error().decode()
 
 
 def test_python_binding_rejects_mismatched_grid(L):

@@ -24,15 +24,15 @@ def _built():
     vdx.lib()
 
 
-def _run(w, q, k, v):
-    out, lse = vdx.rope3d_attn(q, k, v, (w.T, w.Hg, w.Wg), w.sections, w.theta)
+def _run(w, q, k, v, **kw):
+    out, lse = vdx.rope3d_attn(q, k, v, (w.T, w.Hg, w.Wg), w.sections, w.theta, **kw)
     vdx.sync_check()
     return out, lse
 
 
-def _full_compare(w, dev_qkv=None):
+def _full_compare(w, dev_qkv=None, **kw):
     q, k, v = dev_qkv if dev_qkv is not None else (t.cuda() for t in synth.make_qkv(w))
-    out, lse = _run(w, q, k, v)
+    out, lse = _run(w, q, k, v, **kw)
     ref_o, ref_l = O.rope3d_attention(q, k, v, (w.T, w.Hg, w.Wg), w.sections, w.theta)
     got_o = out.double().cpu().numpy()
     got_l = lse.double().cpu().numpy()
@@ -60,11 +60,32 @@ BF16_GRIDS = [(3, 8, 8), (3, 5, 7), (1, 1, 1), (1, 1, 129), (4, 9, 13), (5, 8, 1
               (7, 40, 1)]
 
 
+K_MODES = {"prepass": vdx.K_ROPE_PREPASS, "fused": vdx.K_ROPE_FUSED}
+
+
+@pytest.mark.parametrize("mode", sorted(K_MODES))
 @pytest.mark.parametrize("grid", BF16_GRIDS, ids=lambda g: "x".join(map(str, g)))
-def test_bf16_small_shapes(grid):
+def test_bf16_small_shapes(grid, mode):
     w = dataclasses.replace(configs.WAN13B_480P, B=2, H=3, T=grid[0], Hg=grid[1], Wg=grid[2], seed=21)
-    mx, mean, lerr = _full_compare(w)
+    mx, mean, lerr = _full_compare(w, k_rope=K_MODES[mode])
     assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
+
+
+def test_bf16_caller_workspace_matches_library_workspace():
+    w = dataclasses.replace(configs.WAN13B_480P, B=2, H=2, T=2, Hg=7, Wg=19, seed=25)
+    q, k, v = (t.cuda() for t in synth.make_qkv(w))
+    nbytes = vdx.workspace_bytes(w.B, w.H, (w.T, w.Hg, w.Wg))
+    assert nbytes == q.numel() * 2
+    ws = torch.empty(nbytes // 2 + 64, dtype=torch.float16, device="cuda")
+    o1, l1 = _run(w, q, k, v, workspace=ws)
+    o2, l2 = _run(w, q, k, v)
+    o3, l3 = _run(w, q, k, v, k_rope=vdx.K_ROPE_FUSED)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    # the two K modes round the same rotated values to fp16: identical scores and output
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)
+    with pytest.raises(vdx.VdxError) as ei:
+        vdx.rope3d_attn(q, k, v, (w.T, w.Hg, w.Wg), workspace=ws[:100])
+    assert ei.value.status == 1
 
 
 def test_bf16_custom_sections_theta_scale():
@@ -106,9 +127,9 @@ def test_bf16_deterministic_and_guard_bands():
     assert none is None and torch.equal(out2, out)
 
 
-def _sampled_compare(w, rows=512):
+def _sampled_compare(w, rows=512, **kw):
     q, k, v = synth.make_qkv(w, device="cuda")
-    out, lse = _run(w, q, k, v)
+    out, lse = _run(w, q, k, v, **kw)
     sel = synth.sample_rows(w, rows)
     ref_o, ref_l = O.rope3d_attention_rows(q, k, v, (w.T, w.Hg, w.Wg), sel, w.sections, w.theta)
     b = torch.tensor([r[0] for r in sel], device="cuda")
@@ -125,5 +146,12 @@ def _sampled_compare(w, rows=512):
                                configs.LONG_STRESS], ids=lambda w: w.name)
 def test_full_size_configs_sampled(w):
     mx, mean, lerr = _sampled_compare(w)
+    print(f"{w.name}: out max {mx:.3e} mean {mean:.3e} lse max {lerr:.3e}")
+    assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
+
+
+def test_full_size_fused_k_mode_sampled():
+    w = configs.WAN13B_480P
+    mx, mean, lerr = _sampled_compare(w, k_rope=vdx.K_ROPE_FUSED)
     print(f"{w.name}: out max {mx:.3e} mean {mean:.3e} lse max {lerr:.3e}")
     assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)

@@ -3,4 +3,5 @@ GB300 (sm_103a).  The computation lives in libvdx.so (C ABI, include/vdx.h); thi
 holds the ctypes binding, the build step, the measured workloads and the seeded input recipe.
 """
 from ._binding import (VdxError, lib, rope3d_attn, sync_check, shutdown, version,  # noqa: F401
-                       SIGNATURES, LIB_PATH)
+                       workspace_bytes, SIGNATURES, LIB_PATH, K_ROPE_DEFAULT, K_ROPE_PREPASS,
+                       K_ROPE_FUSED)

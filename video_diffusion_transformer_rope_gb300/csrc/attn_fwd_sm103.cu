@@ -1,37 +1,44 @@
-// Warp-specialised flash-attention forward with fused 3D RoPE for sm_103a (GB300).
+// Warp-specialised flash-attention forward with 3D RoPE for sm_103a (GB300), plus the
+// K-rotation prepass it can stream from.
 //
 // Operation: vidax: A Unified JAX Framework for Video Generative Models on Accelerator
 // Meshes, §2 "3D RoPE, 3D VAEs, and flash attention" (rotary 3D positions on Q and K, then
 // attention without materialising the N x N scores).  bf16 in/out, d = 128, fp32 softmax
 // statistics and accumulators.  The rotated Q and K are rounded to fp16 (11-bit significand,
-// 8x finer than bf16) for the QK^T product, whose error then stays well inside the lse
-// tolerance for ordinary activations; P and V enter the PV product as bf16.
+// 8x finer than bf16) for the QK^T product; P and V enter the PV product as bf16.
 //
 // One CTA owns 256 query rows (two 128-row Q tiles) of one (batch, head) and streams every
-// 128-key K/V tile of that head:
+// 128-key K/V tile of that head.  Warp roles (one warpgroup each, registers rebalanced with
+// setmaxnreg once the roles split):
 //
-//   warps 0-3   softmax for Q tile 0   (thread = one query row = one TMEM lane)
-//   warps 4-7   softmax for Q tile 1
-//   warps 8-11  RoPE: rotate Q tiles once, and each K tile in shared memory as it lands
-//               (bf16 in, fp16 out, in place)
-//   warp  12    TMA producer: Q tiles once, then K/V tiles into two 2-stage rings
-//   warp  13    tcgen05 MMA issuer (one thread) and TMEM owner
-//   warps 14-15 idle
+//   WG0  warps 0-3   softmax + epilogue for Q tile 0 (thread = query row = TMEM lane)
+//   WG1  warps 4-7   softmax + epilogue for Q tile 1
+//   WG2  warps 8-11  RoPE: rotate the Q tiles in shared memory as they land (bf16 -> fp16,
+//                    in place); in the fused-K mode also every K tile
+//   WG3  warp 12     TMA producer: Q tiles once, then K/V tiles through the rings
+//        warp 13     tcgen05 MMA issuer (one thread) and TMEM owner; warps 14-15 idle
+//
+// K modes.  Prepass (default): a separate kernel rotates K once per token into an fp16
+// workspace and the attention kernel streams that, so no K rotation sits in the hot loop.
+// Fused: TMA brings raw bf16 K and WG2 rotates each K tile in shared memory before the MMA
+// reads it (every CTA of a head repeats this for every K tile).
 //
 // TMEM (512 columns x 128 lanes, fp32): S0 [0,128)  S1 [128,256)  O0 [256,384)  O1 [384,512).
 // P_i (bf16, two per column) overwrites the first 64 columns of S_i and is the A operand of
 // the PV MMA straight from TMEM.  MMA issue order per key tile j:
 //     S0(j) = Q0 K_j^T ;  O1 += P1(j-1) V_{j-1} ;  S1(j) = Q1 K_j^T ;  O0 += P0(j) V_j
-// so softmax of one Q tile overlaps the tensor-core work of the other.  The online softmax
-// works in the log2 domain (exp2 with scale*log2(e) folded into one FMA) and only rescales
-// O when a row maximum grows by more than 8 (a factor 256), which keeps P <= 256.
+// so softmax of one Q tile overlaps the tensor-core work of the other.  Completion of S_i(j)
+// implies completion of every earlier MMA, so O_i may be rescaled as soon as S_i(j) is seen.
+// The online softmax works in the log2 domain (exp2 with scale*log2(e) folded into one FMA)
+// and only rescales O when a row maximum grows by more than 8 (a factor 256): P <= 256.
 //
-// Shared memory: Q 2x32 KB, K ring 2x32 KB, V ring 2x32 KB, each tile stored as two
-// 128-row x 128-byte halves in the 128-byte-swizzled layout TMA writes; the cos/sin table
-// (when it fits) and the mbarriers follow.
+// Shared memory: Q 2x32 KB, K ring, V ring (32 KB per stage), each tile stored as two
+// 128-row x 128-byte halves in the 128-byte-swizzled layout TMA writes; then (fused mode,
+// when it fits) the cos/sin table, then the mbarriers.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 #include <cmath>
 
@@ -46,18 +53,28 @@ constexpr int kQTiles = 2;               // Q tiles per CTA
 constexpr int kRowsPerCta = kBM * kQTiles;
 constexpr int kBN = 128;                 // keys per K/V tile
 constexpr int kD = 128;
-constexpr int kKStages = 2;
-constexpr int kVStages = 2;
 constexpr int kTileBytes = kBN * kD * 2; // 32 KB
 constexpr int kHalfBytes = kTileBytes / 2;
 constexpr int kThreads = 512;
 constexpr int kTmemCols = 512;
-
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQTiles * kTileBytes;
-constexpr int kOffV = kOffK + kKStages * kTileBytes;
-constexpr int kOffTab = kOffV + kVStages * kTileBytes;
+constexpr int kMaxStages = 3;
 constexpr int kMaxDynSmem = 232448;      // sm_100-family opt-in limit per CTA
+
+// Registers per thread after the split (sum over the 4 warpgroups = 512 x 128 at launch).
+constexpr uint32_t kRegsSoftmax = 192;
+constexpr uint32_t kRegsRope = 56;
+constexpr uint32_t kRegsCtl = 72;
+static_assert(2 * kRegsSoftmax + kRegsRope + kRegsCtl <= 4 * 128, "register split over budget");
+
+template <bool kFusedK>
+struct Layout {
+  static constexpr int kKStages = kFusedK ? 2 : 3;
+  static constexpr int kVStages = 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQTiles * kTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffTab = kOffV + kVStages * kTileBytes;
+};
 
 // Wait sites recorded in the error word when a bounded wait gives up.
 enum : int {
@@ -68,11 +85,11 @@ enum : int {
 struct Ctl {
   uint64_t q_full[kQTiles];
   uint64_t q_ready[kQTiles];
-  uint64_t k_full[kKStages];
-  uint64_t k_ready[kKStages];
-  uint64_t k_empty[kKStages];
-  uint64_t v_full[kVStages];
-  uint64_t v_empty[kVStages];
+  uint64_t k_full[kMaxStages];
+  uint64_t k_ready[kMaxStages];
+  uint64_t k_empty[kMaxStages];
+  uint64_t v_full[kMaxStages];
+  uint64_t v_empty[kMaxStages];
   uint64_t s_full[kQTiles];
   uint64_t p_ready[kQTiles];
   uint64_t o_final;
@@ -144,44 +161,61 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
   }
 }
 
-// Rotate one 128-row tile in place (bf16, swizzled halves).  Thread t of the 128 RoPE
-// threads always touches 16-byte chunk (t & 15) of rows (t >> 4) + 8*it, so its four rotary
-// pairs, and therefore their axes and table columns, are fixed.
+// Which rotary pairs a thread owns.  Thread t of the 128 RoPE threads always touches 16-byte
+// chunk (t & 15) of a 256-byte row, i.e. pairs 4*(t&15) .. +3, so their axes and table
+// columns are fixed per thread.
 struct RopeLane {
   int tab_base[4];   // entry of position 0 for each of the thread's pairs
   int tab_stride[4]; // entries per position step on that pair's axis
   int axis[4];       // 0 = t, 1 = h, 2 = w
-  uint32_t chunk_off;
-  int rsub;
 };
 
-__device__ __forceinline__ RopeLane make_rope_lane(const Params& p, int t) {
+__device__ __forceinline__ RopeLane make_rope_lane(int c16, int half_t, int half_h, int half_w,
+                                                   int off_h, int off_w) {
   RopeLane L;
-  const int c16 = t & 15;
-  const int half = c16 >> 3;
-  const int cc = c16 & 7;
-  L.rsub = t >> 4;
-  L.chunk_off = half * kHalfBytes + L.rsub * 128 + ((cc ^ L.rsub) << 4);
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const int pr = half * 32 + cc * 4 + e;
-    if (pr < p.half_t) {
-      L.axis[e] = 0; L.tab_base[e] = pr; L.tab_stride[e] = p.half_t;
-    } else if (pr < p.half_t + p.half_h) {
-      L.axis[e] = 1; L.tab_base[e] = p.off_h + (pr - p.half_t); L.tab_stride[e] = p.half_h;
+    const int pr = c16 * 4 + e;
+    if (pr < half_t) {
+      L.axis[e] = 0; L.tab_base[e] = pr; L.tab_stride[e] = half_t;
+    } else if (pr < half_t + half_h) {
+      L.axis[e] = 1; L.tab_base[e] = off_h + (pr - half_t); L.tab_stride[e] = half_h;
     } else {
-      L.axis[e] = 2; L.tab_base[e] = p.off_w + (pr - p.half_t - p.half_h);
-      L.tab_stride[e] = p.half_w;
+      L.axis[e] = 2; L.tab_base[e] = off_w + (pr - half_t - half_h); L.tab_stride[e] = half_w;
     }
   }
   return L;
 }
 
-// Rotates bf16 in place into fp16; returns the largest |rotated value| seen.
-__device__ __forceinline__ float rope_tile(const Params& p, const RopeLane& L, uint8_t* tile,
+// Rotate the 4 pairs of one 16-byte chunk (bf16 in) of a token at grid position (pt,ph,pw);
+// returns the fp16 result and folds |rotated| into amax.
+__device__ __forceinline__ uint4 rotate_chunk(uint4 x, const RopeLane& L, int pt, int ph, int pw,
+                                              const float2* __restrict__ tab, float& amax) {
+  uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int pos = L.axis[e] == 0 ? pt : (L.axis[e] == 1 ? ph : pw);
+    const float2 cs = tab[L.tab_base[e] + pos * L.tab_stride[e]];
+    const float x0 = __uint_as_float(w[e] << 16);
+    const float x1 = __uint_as_float(w[e] & 0xffff0000u);
+    const float y0 = fmaf(x0, cs.x, -x1 * cs.y);
+    const float y1 = fmaf(x0, cs.y, x1 * cs.x);
+    amax = fmax3(amax, fabsf(y0), fabsf(y1));
+    w[e] = pack_f16x2_sat(y0, y1);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Rotate one 128-row tile in place (bf16 in, fp16 out, swizzled halves).  Thread t handles
+// chunk (t & 15) of rows (t >> 4) + 8*it; the 8 threads sharing a row hit 8 distinct
+// 16-byte bank groups.
+__device__ __forceinline__ float rope_tile(const Params& p, const RopeLane& L, int t, uint8_t* tile,
                                            int n_first, const float2* __restrict__ tab) {
   float amax = 0.f;
-  int n = n_first + L.rsub;
+  const int c16 = t & 15;
+  const int rsub = t >> 4;
+  const uint32_t chunk_off = (c16 >> 3) * kHalfBytes + rsub * 128 + (((c16 & 7) ^ rsub) << 4);
+  int n = n_first + rsub;
   if (n >= p.N) return amax;
   int pt = n / p.HgWg;
   int rem = n - pt * p.HgWg;
@@ -190,21 +224,8 @@ __device__ __forceinline__ float rope_tile(const Params& p, const RopeLane& L, u
 #pragma unroll 2
   for (int it = 0; it < kBM / 8; ++it) {
     if (n >= p.N) break;
-    uint4* ptr = reinterpret_cast<uint4*>(tile + L.chunk_off + it * 1024);
-    uint4 x = *ptr;
-    uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int pos = L.axis[e] == 0 ? pt : (L.axis[e] == 1 ? ph : pw);
-      const float2 cs = tab[L.tab_base[e] + pos * L.tab_stride[e]];
-      __nv_bfloat162 v2 = *reinterpret_cast<__nv_bfloat162*>(&w[e]);
-      const float x0 = __low2float(v2), x1 = __high2float(v2);
-      const float y0 = fmaf(x0, cs.x, -x1 * cs.y);
-      const float y1 = fmaf(x0, cs.y, x1 * cs.x);
-      amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
-      w[e] = pack_f16x2_sat(y0, y1);
-    }
-    *ptr = make_uint4(w[0], w[1], w[2], w[3]);
+    uint4* ptr = reinterpret_cast<uint4*>(tile + chunk_off + it * 1024);
+    *ptr = rotate_chunk(*ptr, L, pt, ph, pw, tab, amax);
     n += 8;
     pw += 8;
     while (pw >= p.Wg) { pw -= p.Wg; ++ph; }
@@ -213,14 +234,18 @@ __device__ __forceinline__ float rope_tile(const Params& p, const RopeLane& L, u
   return amax;
 }
 
+template <bool kFusedK>
 __global__ void __launch_bounds__(kThreads, 1)
-attn_fwd_bf16_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
+attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  using Lo = Layout<kFusedK>;
+  constexpr int kKStages = Lo::kKStages;
+  constexpr int kVStages = Lo::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + p.ctl_off);
-  float2* tab_s = reinterpret_cast<float2*>(smem + kOffTab);
+  float2* tab_s = reinterpret_cast<float2*>(smem + Lo::kOffTab);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -233,9 +258,9 @@ attn_fwd_bf16_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   const int q0 = qblk * kRowsPerCta;
   const int nkv = (p.N + kBN - 1) / kBN;
 
-  const uint32_t sQ = smem_addr(smem + kOffQ);
-  const uint32_t sK = smem_addr(smem + kOffK);
-  const uint32_t sV = smem_addr(smem + kOffV);
+  const uint32_t sQ = smem_addr(smem + Lo::kOffQ);
+  const uint32_t sK = smem_addr(smem + Lo::kOffK);
+  const uint32_t sV = smem_addr(smem + Lo::kOffV);
 
   if (tid == 0) {
     for (int i = 0; i < kQTiles; ++i) {
@@ -261,7 +286,7 @@ attn_fwd_bf16_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  if (p.table_in_smem) {
+  if (kFusedK && p.table_in_smem) {
     for (int i = tid; i < p.table_entries; i += kThreads) tab_s[i] = p.table[i];
   }
   tc_fence_before_sync();
@@ -270,9 +295,10 @@ attn_fwd_bf16_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   const uint32_t tmem = ctl->tmem_base;
   volatile int* abort_flag = &ctl->abort_flag;
 
-  if (warp == 12) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+  if (warp >= 12) {
+    regs_decrease<kRegsCtl>();
+    if (warp == 12 && lane == 0) {
+      // ---------------------------------------------------------- TMA producer
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
@@ -318,11 +344,8 @@ attn_fwd_bf16_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int uses = v_issued > s ? (v_issued - 1 - s) / kVStages + 1 : 0;
         if (uses > 0) drain_wait(smem_addr(&ctl->v_full[s]), (uses - 1) & 1);
       }
-    }
-    __syncwarp();
-  } else if (warp == 13) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 13 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t kIdQK = idesc_f16kind_f32acc(kBM, kBN, 0, 0);   // fp16 Q', K'
       constexpr uint32_t kIdPV = idesc_f16kind_f32acc(kBM, kD, 1, 1);   // bf16 P, V (MN-major)
       const uint32_t tS0 = tmem + 0, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
@@ -331,7 +354,8 @@ attn_fwd_bf16_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       tc_fence_after_sync();
       for (int j = 0; ok && j < nkv; ++j) {
         const int ks = j % kKStages;
-        if (!(ok = mbar_wait(smem_addr(&ctl->k_ready[ks]), (j / kKStages) & 1, abort_flag, kSiteKReady)))
+        const uint32_t kbar = kFusedK ? smem_addr(&ctl->k_ready[ks]) : smem_addr(&ctl->k_full[ks]);
+        if (!(ok = mbar_wait(kbar, (j / kKStages) & 1, abort_flag, kFusedK ? kSiteKReady : kSiteKFull)))
           break;
         tc_fence_after_sync();
         const uint32_t kt = sK + ks * kTileBytes;
@@ -366,51 +390,72 @@ attn_fwd_bf16_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       drain_wait(smem_addr(&ctl->o_final), 0);
     }
     __syncwarp();
-  } else if (warp >= 8 && warp < 12) {
-    // ------------------------------------------------------------ RoPE on Q and K tiles
-    const float2* tab = p.table_in_smem ? tab_s : p.table;
-    const RopeLane L = make_rope_lane(p, tid - 256);
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ RoPE on Q (and K tiles)
+    regs_decrease<kRegsRope>();
+    const int t = tid - 256;
+    const float2* tab = (kFusedK && p.table_in_smem) ? tab_s : p.table;
+    const RopeLane L = make_rope_lane(t & 15, p.half_t, p.half_h, p.half_w, p.off_h, p.off_w);
     bool ok = true;
     float amax = 0.f;
     for (int i = 0; i < kQTiles && ok; ++i) {
       if (!(ok = mbar_wait(smem_addr(&ctl->q_full[i]), 0, abort_flag, kSiteQFull))) break;
-      amax = fmaxf(amax, rope_tile(p, L, smem + kOffQ + i * kTileBytes, q0 + i * kBM, tab));
+      amax = fmaxf(amax, rope_tile(p, L, t, smem + Lo::kOffQ + i * kTileBytes, q0 + i * kBM, tab));
       fence_proxy_async_smem();
       mbar_arrive(smem_addr(&ctl->q_ready[i]));
     }
-    for (int j = 0; ok && j < nkv; ++j) {
-      const int ks = j % kKStages;
-      if (!(ok = mbar_wait(smem_addr(&ctl->k_full[ks]), (j / kKStages) & 1, abort_flag, kSiteKFull)))
-        break;
-      amax = fmaxf(amax, rope_tile(p, L, smem + kOffK + ks * kTileBytes, j * kBN, tab));
-      fence_proxy_async_smem();
-      mbar_arrive(smem_addr(&ctl->k_ready[ks]));
+    if (kFusedK) {
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int ks = j % kKStages;
+        if (!(ok = mbar_wait(smem_addr(&ctl->k_full[ks]), (j / kKStages) & 1, abort_flag, kSiteKFull)))
+          break;
+        amax = fmaxf(amax, rope_tile(p, L, t, smem + Lo::kOffK + ks * kTileBytes, j * kBN, tab));
+        fence_proxy_async_smem();
+        mbar_arrive(smem_addr(&ctl->k_ready[ks]));
+      }
     }
     if (!(amax <= 65504.f)) atomicOr(&g_error_word, 2u);
-  } else if (warp < 8) {
+  } else {
     // ------------------------------------------------------------ softmax + epilogue
+    regs_increase<kRegsSoftmax>();
     const int qi = warp >> 2;
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_bits = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_bits + 128 * qi;
     const uint32_t tO = tmem + lane_bits + 256 + 128 * qi;
     const float c = p.scale_log2;
+    const uint64_t c2 = f32x2(c, c);
     float m_run = -INFINITY;
     float l_run = 0.f;
     bool ok = true;
-    uint32_t r[32];
     for (int j = 0; j < nkv; ++j) {
       if (!(ok = mbar_wait(smem_addr(&ctl->s_full[qi]), j & 1, abort_flag, kSiteSFull))) break;
       tc_fence_after_sync();
-      const int valid = min(kBN, p.N - j * kBN);
-      float mx = -INFINITY;
+      uint32_t s[128];
+      tmem_ld128(tS, s);
+      const int valid = p.N - j * kBN;
+      if (valid < kBN) {             // ragged last tile: keys beyond N weigh nothing
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        tmem_ld32(tS + ch * 32, r);
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (ch * 32 + e < valid) mx = fmaxf(mx, __uint_as_float(r[e]));
+        for (int e = 0; e < 128; ++e)
+          if (e >= valid) s[e] = 0xff800000u;
       }
+      // row maximum: 16 independent 3-input max chains, then a short tree
+      float mx16[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        mx16[i] = fmax3(__uint_as_float(s[i]), __uint_as_float(s[i + 16]), __uint_as_float(s[i + 32]));
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        mx16[i] = fmax3(mx16[i], __uint_as_float(s[i + 48]), __uint_as_float(s[i + 64]));
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        mx16[i] = fmax3(mx16[i], __uint_as_float(s[i + 80]), __uint_as_float(s[i + 96]));
+#pragma unroll
+      for (int i = 0; i < 16; ++i) mx16[i] = fmaxf(mx16[i], __uint_as_float(s[i + 112]));
+#pragma unroll
+      for (int i = 0; i < 5; ++i) mx16[i] = fmax3(mx16[i], mx16[i + 5], mx16[i + 10]);
+      const float mx = fmax3(fmax3(mx16[0], mx16[1], mx16[2]), fmax3(mx16[3], mx16[4], mx16[15]),
+                             -INFINITY);
       const float m_new = fmaxf(m_run, mx * c);
       const bool resc = m_new > m_run + 8.0f;
       float alpha = 1.f;
@@ -419,23 +464,32 @@ attn_fwd_bf16_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         l_run *= alpha;
         m_run = m_new;
       }
-      float lsum = 0.f;
+      // p = 2^(s*c - m), packed in pairs; row sum in 4 packed accumulators
+      const uint64_t negm2 = f32x2(-m_run, -m_run);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+      uint32_t pk[64];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        tmem_ld32(tS + ch * 32, r);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e2 = 0; e2 < 16; ++e2) {
-          const int e = 2 * e2;
-          const float p0 = (ch * 32 + e < valid) ? ex2_approx(fmaf(__uint_as_float(r[e]), c, -m_run)) : 0.f;
-          const float p1 = (ch * 32 + e + 1 < valid) ? ex2_approx(fmaf(__uint_as_float(r[e + 1]), c, -m_run)) : 0.f;
-          lsum += p0 + p1;
-          pk[e2] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tS + ch * 16, pk);
+      for (int e2 = 0; e2 < 64; ++e2) {
+        const uint64_t a = ffma2(f32x2(__uint_as_float(s[2 * e2]), __uint_as_float(s[2 * e2 + 1])), c2, negm2);
+        float a0, a1;
+        f32x2_split(a, a0, a1);
+        const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+        acc[e2 & 3] = fadd2(acc[e2 & 3], f32x2(p0, p1));
+        pk[e2] = pack_bf16x2(p0, p1);
       }
-      l_run += lsum;
+      {
+        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
+        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
+        tmem_st32(tS, lo);
+        tmem_st32(tS + 32, hi);
+      }
+      const uint64_t acc01 = fadd2(acc[0], acc[1]);
+      const uint64_t acc23 = fadd2(acc[2], acc[3]);
+      float l0, l1;
+      f32x2_split(fadd2(acc01, acc23), l0, l1);
+      l_run += l0 + l1;
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        uint32_t r[32];
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
           tmem_ld32(tO + ch * 32, r);
@@ -455,6 +509,7 @@ attn_fwd_bf16_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const bool live = n < p.N;
       const float inv_l = 1.f / l_run;
       __nv_bfloat16* orow = p.out + ((static_cast<size_t>(b) * p.N + (live ? n : 0)) * p.H + h) * kD;
+      uint32_t r[32];
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
         tmem_ld32(tO + ch * 32, r);
@@ -482,20 +537,46 @@ attn_fwd_bf16_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   }
 }
 
-}  // namespace
-
-cudaError_t read_and_clear_error_word_sm103(unsigned int* word) {
-  cudaError_t e = cudaMemcpyFromSymbol(word, g_error_word, sizeof(unsigned int));
-  if (e != cudaSuccess || *word == 0) return e;
-  const unsigned int zero = 0;
-  return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+// K prepass: rotate every token of K once (bf16 in, fp16 out, same [B, N, H, d] layout).
+// One thread per 16-byte chunk; the grid stride is a multiple of 16 chunks, so each thread
+// keeps one chunk column (and its four rotary pairs) throughout.
+__global__ void __launch_bounds__(256)
+rope3d_k_prepass(const uint4* __restrict__ k, uint4* __restrict__ kr, const Params p,
+                 uint32_t n_chunks) {
+  const uint32_t stride = gridDim.x * blockDim.x;
+  uint32_t c = blockIdx.x * blockDim.x + threadIdx.x;
+  const RopeLane L = make_rope_lane(static_cast<int>(c & 15), p.half_t, p.half_h, p.half_w,
+                                    p.off_h, p.off_w);
+  float amax = 0.f;
+  for (; c < n_chunks; c += stride) {
+    const uint32_t row = c >> 4;                       // (b*N + n)*H + h
+    const uint32_t n = (row / static_cast<uint32_t>(p.H)) % static_cast<uint32_t>(p.N);
+    const int pt = static_cast<int>(n) / p.HgWg;
+    const int rem = static_cast<int>(n) - pt * p.HgWg;
+    const int ph = rem / p.Wg;
+    const int pw = rem - ph * p.Wg;
+    const uint4 x = __ldg(k + c);
+    kr[c] = rotate_chunk(x, L, pt, ph, pw, p.table, amax);
+  }
+  if (!(amax <= 65504.f)) atomicOr(&g_error_word, 2u);
 }
 
-cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, cudaStream_t stream,
-                                   const char** what) {
-  *what = nullptr;
-  CUtensorMap maps[3];
-  const void* srcs[3] = {pr.q, pr.k, pr.v};
+void fill_params(const Problem& pr, Params* p) {
+  *p = Params{};
+  p->B = pr.B; p->H = pr.H; p->N = pr.N; p->Hg = pr.Hg; p->Wg = pr.Wg; p->HgWg = pr.Hg * pr.Wg;
+  p->half_t = pr.half_t; p->half_h = pr.half_h; p->half_w = pr.half_w;
+  p->off_h = pr.T * pr.half_t;
+  p->off_w = p->off_h + pr.Hg * pr.half_h;
+  p->table_entries = pr.table_entries;
+  p->n_qblk = (pr.N + kRowsPerCta - 1) / kRowsPerCta;
+  p->scale_log2 = pr.scale * 1.4426950408889634f;
+  p->table = pr.table;
+  p->out = static_cast<__nv_bfloat16*>(pr.out);
+  p->lse = pr.lse;
+}
+
+CUresult encode_bhnd(EncodeTiledFn encode, CUtensorMap* map, const void* base,
+                     CUtensorMapDataType dtype, const Problem& pr) {
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(pr.H),
                               static_cast<cuuint64_t>(pr.N), static_cast<cuuint64_t>(pr.B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kD) * 2,
@@ -503,39 +584,28 @@ cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, cuda
                                  static_cast<cuuint64_t>(pr.N) * pr.H * kD * 2};
   const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBN), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  for (int i = 0; i < 3; ++i) {
-    CUresult r = encode(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(srcs[i]),
-                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-      *what = "cuTensorMapEncodeTiled failed";
-      return cudaErrorInvalidValue;
-    }
-  }
-  Params p{};
-  p.B = pr.B; p.H = pr.H; p.N = pr.N; p.Hg = pr.Hg; p.Wg = pr.Wg; p.HgWg = pr.Hg * pr.Wg;
-  p.half_t = pr.half_t; p.half_h = pr.half_h; p.half_w = pr.half_w;
-  p.off_h = pr.T * pr.half_t;
-  p.off_w = p.off_h + pr.Hg * pr.half_h;
-  p.table_entries = pr.table_entries;
-  p.n_qblk = (pr.N + kRowsPerCta - 1) / kRowsPerCta;
-  p.scale_log2 = pr.scale * 1.4426950408889634f;
-  p.table = pr.table;
-  p.out = static_cast<__nv_bfloat16*>(pr.out);
-  p.lse = pr.lse;
+  return encode(map, dtype, 4, const_cast<void*>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+template <bool kFusedK>
+cudaError_t launch_attn(const Problem& pr, Params p, const CUtensorMap* maps, cudaStream_t stream,
+                        const char** what) {
+  using Lo = Layout<kFusedK>;
   const int tab_bytes = ((pr.table_entries * 8) + 15) & ~15;
   const int ctl_bytes = (static_cast<int>(sizeof(Ctl)) + 15) & ~15;
-  int smem = kOffTab + tab_bytes + ctl_bytes + 1024;
-  if (smem <= kMaxDynSmem) {
+  int smem = Lo::kOffTab + tab_bytes + ctl_bytes + 1024;
+  if (kFusedK && smem <= kMaxDynSmem) {
     p.table_in_smem = 1;
-    p.ctl_off = kOffTab + tab_bytes;
+    p.ctl_off = Lo::kOffTab + tab_bytes;
   } else {
     p.table_in_smem = 0;
-    p.ctl_off = kOffTab;
-    smem = kOffTab + ctl_bytes + 1024;
+    p.ctl_off = Lo::kOffTab;
+    smem = Lo::kOffTab + ctl_bytes + 1024;
   }
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_sm103, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_sm103<kFusedK>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) {
     *what = "cudaFuncSetAttribute(max dynamic shared memory) failed";
     return e;
@@ -545,10 +615,63 @@ cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, cuda
     *what = "grid too large";
     return cudaErrorInvalidValue;
   }
-  attn_fwd_bf16_sm103<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(maps[0], maps[1], maps[2], p);
+  attn_fwd_sm103<kFusedK><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(maps[0], maps[1], maps[2], p);
   e = cudaGetLastError();
-  if (e != cudaSuccess) *what = "kernel launch failed";
+  if (e != cudaSuccess) *what = "attention kernel launch failed";
   return e;
+}
+
+}  // namespace
+
+cudaError_t read_and_clear_error_word_sm103(unsigned int* word) {
+  cudaError_t e = cudaMemcpyFromSymbol(word, g_error_word, sizeof(unsigned int));
+  if (e != cudaSuccess || *word == 0) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+}
+
+size_t k_prepass_workspace_bytes(const Problem& pr) {
+  return static_cast<size_t>(pr.B) * pr.N * pr.H * kD * 2;
+}
+
+cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, bool fused_k,
+                                   void* workspace, cudaStream_t stream, const char** what) {
+  *what = nullptr;
+  Params p;
+  fill_params(pr, &p);
+  CUtensorMap maps[3];
+  const void* kbase = pr.k;
+  if (!fused_k) {
+    const size_t chunks = k_prepass_workspace_bytes(pr) / 16;
+    if (chunks >= 0x80000000ull) {
+      *what = "K prepass: tensor too large";
+      return cudaErrorInvalidValue;
+    }
+    int sms = 148;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long want = (static_cast<long long>(chunks) + 255) / 256;
+    const unsigned blocks = static_cast<unsigned>(std::min<long long>(want, static_cast<long long>(sms) * 8));
+    rope3d_k_prepass<<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(pr.k),
+                                                  static_cast<uint4*>(workspace), p,
+                                                  static_cast<uint32_t>(chunks));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      *what = "K prepass launch failed";
+      return e;
+    }
+    kbase = workspace;
+  }
+  if (encode_bhnd(encode, &maps[0], pr.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr) != CUDA_SUCCESS ||
+      encode_bhnd(encode, &maps[1], kbase,
+                  fused_k ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr) != CUDA_SUCCESS ||
+      encode_bhnd(encode, &maps[2], pr.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr) != CUDA_SUCCESS) {
+    *what = "cuTensorMapEncodeTiled failed";
+    return cudaErrorInvalidValue;
+  }
+  return fused_k ? launch_attn<true>(pr, p, maps, stream, what)
+                 : launch_attn<false>(pr, p, maps, stream, what);
 }
 
 }  // namespace vdx

@@ -42,6 +42,11 @@ struct TableEntry {
 };
 std::mutex g_mu;
 std::map<TableKey, TableEntry> g_tables;
+struct Workspace {
+  void* ptr;
+  size_t bytes;
+};
+std::map<int, Workspace> g_workspace;     // library-owned K-prepass scratch, per device
 vdx::EncodeTiledFn g_encode = nullptr;
 
 // Entries: [T][st/2] then [Hg][sh/2] then [Wg][sw/2], each (cos, sin) of pos * theta^(-2j/S).
@@ -105,6 +110,29 @@ vdx_status get_encode(vdx::EncodeTiledFn* fn) {
   return VDX_OK;
 }
 
+// Library-owned scratch of at least `bytes` on the current device (grow-only; growing frees
+// the old buffer, which cudaFree does only after work already queued on the device).
+vdx_status get_workspace(size_t bytes, void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(VDX_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  std::lock_guard<std::mutex> lock(g_mu);
+  Workspace& w = g_workspace[dev];
+  if (w.bytes < bytes) {
+    if (w.ptr) cudaFree(w.ptr);
+    w.ptr = nullptr;
+    w.bytes = 0;
+    e = cudaMalloc(&w.ptr, bytes);
+    if (e != cudaSuccess) {
+      w.ptr = nullptr;
+      return fail(VDX_ERR_CUDA, "cudaMalloc(workspace, %zu bytes): %s", bytes, cudaGetErrorString(e));
+    }
+    w.bytes = bytes;
+  }
+  *out = w.ptr;
+  return VDX_OK;
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
@@ -161,22 +189,57 @@ vdx_status prepare(const void* q, const void* k, const void* v, void* out, float
 
 extern "C" {
 
-vdx_status vdx_rope3d_attn(const void* q, const void* k, const void* v, void* out, float* lse,
-                           int B, int H, int T, int Hgrid, int Wgrid, int d, int sec_t, int sec_h,
-                           int sec_w, double theta, float scale, void* stream) {
+vdx_status vdx_rope3d_attn_ex(const void* q, const void* k, const void* v, void* out, float* lse,
+                              int B, int H, int T, int Hgrid, int Wgrid, int d, int sec_t,
+                              int sec_h, int sec_w, double theta, float scale,
+                              const vdx_attn_options* opt, void* stream) {
   t_last_error.clear();
   if (d != 128) return fail(VDX_ERR_UNSUPPORTED, "bf16 path supports head_dim 128 only (got %d)", d);
+  const int mode = opt ? opt->k_rope : VDX_K_ROPE_DEFAULT;
+  if (mode != VDX_K_ROPE_DEFAULT && mode != VDX_K_ROPE_PREPASS && mode != VDX_K_ROPE_FUSED)
+    return fail(VDX_ERR_ARG, "unknown k_rope mode %d", mode);
+  const bool fused = mode == VDX_K_ROPE_FUSED;
   vdx::Problem p{};
   vdx_status s = prepare(q, k, v, out, lse, B, H, T, Hgrid, Wgrid, d, sec_t, sec_h, sec_w, theta,
                          scale, 2, &p);
   if (s != VDX_OK) return s;
+  void* ws = nullptr;
+  if (!fused) {
+    const size_t need = vdx::k_prepass_workspace_bytes(p);
+    if (opt && opt->workspace) {
+      if (opt->workspace_bytes < need)
+        return fail(VDX_ERR_ARG, "workspace of %zu bytes is smaller than the %zu needed",
+                    opt->workspace_bytes, need);
+      if (reinterpret_cast<uintptr_t>(opt->workspace) & 15)
+        return fail(VDX_ERR_ALIGN, "workspace is not 16-byte aligned");
+      const size_t bytes = need;
+      if (overlaps(opt->workspace, bytes, q, bytes) || overlaps(opt->workspace, bytes, k, bytes) ||
+          overlaps(opt->workspace, bytes, v, bytes) || overlaps(opt->workspace, bytes, out, bytes))
+        return fail(VDX_ERR_ARG, "workspace overlaps q, k, v or out");
+      ws = opt->workspace;
+    } else if ((s = get_workspace(need, &ws)) != VDX_OK) {
+      return s;
+    }
+  }
   vdx::EncodeTiledFn enc = nullptr;
   if ((s = get_encode(&enc)) != VDX_OK) return s;
   const char* what = nullptr;
-  cudaError_t e = vdx::launch_attn_bf16_sm103(p, enc, static_cast<cudaStream_t>(stream), &what);
+  cudaError_t e = vdx::launch_attn_bf16_sm103(p, enc, fused, ws, static_cast<cudaStream_t>(stream), &what);
   if (e != cudaSuccess)
     return fail(VDX_ERR_CUDA, "%s: %s", what ? what : "launch", cudaGetErrorString(e));
   return VDX_OK;
+}
+
+vdx_status vdx_rope3d_attn(const void* q, const void* k, const void* v, void* out, float* lse,
+                           int B, int H, int T, int Hgrid, int Wgrid, int d, int sec_t, int sec_h,
+                           int sec_w, double theta, float scale, void* stream) {
+  return vdx_rope3d_attn_ex(q, k, v, out, lse, B, H, T, Hgrid, Wgrid, d, sec_t, sec_h, sec_w,
+                            theta, scale, nullptr, stream);
+}
+
+size_t vdx_rope3d_workspace_bytes(int B, int H, int T, int Hgrid, int Wgrid, int d) {
+  if (B < 1 || H < 1 || T < 1 || Hgrid < 1 || Wgrid < 1 || d < 1) return 0;
+  return static_cast<size_t>(B) * T * Hgrid * Wgrid * H * d * 2;
 }
 
 vdx_status vdx_rope3d_attn_f32(const float* q, const float* k, const float* v, float* out,
@@ -220,8 +283,13 @@ void vdx_shutdown(void) {
     cudaSetDevice(std::get<0>(kv.first));
     cudaFree(kv.second.ptr);
   }
+  for (auto& kv : g_workspace) {
+    cudaSetDevice(kv.first);
+    if (kv.second.ptr) cudaFree(kv.second.ptr);
+  }
   cudaSetDevice(cur);
   g_tables.clear();
+  g_workspace.clear();
 }
 
 int vdx_version(void) { return 100; }

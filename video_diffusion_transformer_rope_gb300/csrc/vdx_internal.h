@@ -29,8 +29,12 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-cudaError_t launch_attn_bf16_sm103(const Problem& p, EncodeTiledFn encode, cudaStream_t stream,
-                                   const char** what);
+// fused_k = false: K is first rotated once into `workspace` (fp16, [B, N, H, d], at least
+// k_prepass_workspace_bytes(p) bytes, 16-byte aligned) by a prepass kernel on the same stream.
+// fused_k = true: every CTA rotates its K tiles in shared memory; `workspace` is unused.
+cudaError_t launch_attn_bf16_sm103(const Problem& p, EncodeTiledFn encode, bool fused_k,
+                                   void* workspace, cudaStream_t stream, const char** what);
+size_t k_prepass_workspace_bytes(const Problem& p);
 
 // Read the tensor-core kernel's device error word (synchronous) and reset it to 0.
 cudaError_t read_and_clear_error_word_sm103(unsigned int* word);
