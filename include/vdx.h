@@ -95,6 +95,27 @@ vdx_status vdx_rope3d_attn_f32(const float* q, const float* k, const float* v, f
                                int sec_t, int sec_h, int sec_w, double theta, float scale,
                                void* stream);
 
+/* ---- No-allocation variant.  The vidax page has no counterpart: this is a deployment aid
+ * for callers that cannot allocate device memory at call time (a frozen memory pool, an
+ * allocator-free embedding, a host that sizes every buffer up front).  Same operation,
+ * arguments, layouts and K-prepass arithmetic as vdx_rope3d_attn, but the cos/sin table and
+ * the rotated keys live in one fixed static device array of the library instead of memory
+ * allocated on first use, and the call makes no cudaMalloc/cudaFree.
+ *   Limit: B*N*H*d*2 <= VDX_NOALLOC_MAX_WORKSPACE_BYTES and T*sec_t/2 + Hgrid*sec_h/2 +
+ *   Wgrid*sec_w/2 <= VDX_NOALLOC_MAX_TABLE_ENTRIES; larger problems return
+ *   VDX_ERR_UNSUPPORTED.
+ *   The array (about 64 MiB) is held on every GPU that loads the library until exit.
+ *   Every call shares it and it keeps the last call's contents, so calls that may overlap on
+ *   the GPU (unordered streams) race; order them or use vdx_rope3d_attn_ex with a workspace.
+ *   The first call on each device looks up the array's device address (make it before any
+ *   stream capture). */
+#define VDX_NOALLOC_MAX_WORKSPACE_BYTES (64ull << 20)
+#define VDX_NOALLOC_MAX_TABLE_ENTRIES 8192
+vdx_status vdx_rope3d_attn_noalloc(const void* q, const void* k, const void* v, void* out,
+                                   float* lse, int B, int H, int T, int Hgrid, int Wgrid, int d,
+                                   int sec_t, int sec_h, int sec_w, double theta, float scale,
+                                   void* stream);
+
 /* Synchronise `stream`, then read and clear the device error word.  Returns VDX_OK,
  * VDX_ERR_TIMEOUT (a kernel gave up on a pipeline wait; the output of that call is
  * undefined), VDX_ERR_RANGE (a rotated q/k value was clamped to the fp16 range; the output

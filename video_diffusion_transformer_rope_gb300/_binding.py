@@ -29,6 +29,7 @@ SIGNATURES = {
                                 ctypes.POINTER(AttnOptions), _p]),
     "vdx_rope3d_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i]),
     "vdx_rope3d_attn_f32": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f, _p]),
+    "vdx_rope3d_attn_noalloc": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f, _p]),
     "vdx_sync_check": (_i, [_p]),
     "vdx_last_error": (ctypes.c_char_p, []),
     "vdx_shutdown": (None, []),

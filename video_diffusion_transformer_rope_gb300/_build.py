@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libvdx.so")
-SOURCES = ["vdx_capi.cu", "attn_fwd_sm103.cu", "attn_fwd_f32.cu"]
+SOURCES = ["vdx_capi.cu", "attn_fwd_sm103.cu", "attn_fwd_f32.cu", "vdx_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I", INCLUDE, "-I", CSRC]

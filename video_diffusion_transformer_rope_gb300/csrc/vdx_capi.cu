@@ -187,6 +187,10 @@ vdx_status prepare(const void* q, const void* k, const void* v, void* out, float
 
 }  // namespace
 
+namespace vdx {
+void set_last_error(const char* message) { t_last_error = message; }
+}  // namespace vdx
+
 extern "C" {
 
 vdx_status vdx_rope3d_attn_ex(const void* q, const void* k, const void* v, void* out, float* lse,

@@ -39,6 +39,9 @@ size_t k_prepass_workspace_bytes(const Problem& p);
 // Read the tensor-core kernel's device error word (synchronous) and reset it to 0.
 cudaError_t read_and_clear_error_word_sm103(unsigned int* word);
 
+// Set the message vdx_last_error() returns on this host thread (vdx_capi.cu).
+void set_last_error(const char* message);
+
 // fp32, d in {64, 128}, CUDA-core kernel (attn_fwd_f32.cu).
 cudaError_t launch_attn_f32(const Problem& p, cudaStream_t stream);
 
