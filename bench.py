@@ -184,7 +184,7 @@ def run_reference(args, w):
 
 
 def _config(w, k_rope="prepass"):
-    return {"workload": w.name, "k_rope": k_rope, "B": w.B, "heads": w.H, "head_dim": w.d,
+    return {"workload": w.name, "k_rope": k_rope, "qk_operands": w.qk, "B": w.B, "heads": w.H, "head_dim": w.d,
             "grid": f"{w.T}x{w.Hg}x{w.Wg}", "N": w.N,
             "sections": "/".join(map(str, w.sections)), "theta": w.theta,
             "l2": "inputs larger than L2 (q, k, v 1.55 GB each); no flush",
@@ -217,12 +217,13 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream()
 
     k_mode = {"prepass": vdx.K_ROPE_PREPASS, "fused": vdx.K_ROPE_FUSED}[args.k_rope]
-    k_ws = torch.empty(vdx.workspace_bytes(w.B, w.H, grid, w.d) // 2, dtype=torch.float16,
+    qk = vdx.QK_SPLIT if w.qk == "split" else vdx.QK_FP16
+    k_ws = torch.empty(vdx.workspace_bytes(w.B, w.H, grid, w.d, qk) // 2, dtype=torch.float16,
                        device=dev) if args.k_rope == "prepass" else None
 
     def step():
         vdx.rope3d_attn(q, k, v, grid, w.sections, w.theta, out=out, lse=lse, stream=stream,
-                        k_rope=k_mode, workspace=k_ws)
+                        k_rope=k_mode, workspace=k_ws, qk_precision=qk)
 
     for _ in range(args.warmup):
         step()

@@ -56,8 +56,15 @@ typedef enum {
 #define VDX_K_ROPE_FUSED 2    /* each CTA rotates every K tile in shared memory as it lands
                                  (no workspace; the rotation is repeated per query block)     */
 
+/* Precision of the rotated Q/K operands of QK^T on the bf16 path. */
+#define VDX_QK_FP16 0         /* one fp16 value per rotated element (default; fastest)          */
+#define VDX_QK_SPLIT 1        /* fp16 hi + lo per element and three products (~22 significant
+                                 bits): for activations whose logits reach the hundreds; about
+                                 half the speed; needs the K prepass and twice its workspace  */
+
 typedef struct vdx_attn_options {
   int k_rope;               /* one of VDX_K_ROPE_*                                              */
+  int qk_precision;         /* one of VDX_QK_*                                                  */
   void* workspace;          /* device scratch for the prepass, >= vdx_rope3d_workspace_bytes()
                                bytes, 16-byte aligned, not overlapping q/k/v/out; NULL = a
                                library-owned per-device buffer (allocated or grown with
@@ -78,15 +85,17 @@ vdx_status vdx_rope3d_attn(const void* q, const void* k, const void* v, void* ou
                            int sec_t, int sec_h, int sec_w, double theta, float scale,
                            void* stream);
 
-/* Same as vdx_rope3d_attn with explicit options (NULL = defaults: K prepass, library-owned
- * workspace). */
+/* Same as vdx_rope3d_attn with explicit options (NULL = defaults: K prepass, fp16 QK operands,
+ * library-owned workspace). */
 vdx_status vdx_rope3d_attn_ex(const void* q, const void* k, const void* v, void* out, float* lse,
                               int B, int H, int T, int Hgrid, int Wgrid, int d,
                               int sec_t, int sec_h, int sec_w, double theta, float scale,
                               const vdx_attn_options* opt, void* stream);
 
-/* Bytes of workspace the K prepass needs for this problem (B*N*H*d*2), 0 for invalid sizes. */
-size_t vdx_rope3d_workspace_bytes(int B, int H, int T, int Hgrid, int Wgrid, int d);
+/* Bytes of workspace the K prepass needs for this problem: B*N*H*d*2, twice that with
+ * VDX_QK_SPLIT; 0 for invalid sizes. */
+size_t vdx_rope3d_workspace_bytes(int B, int H, int T, int Hgrid, int Wgrid, int d,
+                                  int qk_precision);
 
 /* fp32 path (CUDA cores, fp32 arithmetic throughout).  Same operation and rules; q, k, v,
  * out are float [B, N, H, d]; d must be 64 or 128. */

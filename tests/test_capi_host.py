@@ -70,16 +70,22 @@ def test_rejects_bad_arguments_without_cuda(L, kw, status, msg):
 
 
 def test_workspace_bytes(L):
-    assert L.vdx_rope3d_workspace_bytes(2, 40, 21, 45, 80, 128) == 2 * 75600 * 40 * 128 * 2
-    assert L.vdx_rope3d_workspace_bytes(0, 40, 21, 45, 80, 128) == 0
+    assert L.vdx_rope3d_workspace_bytes(2, 40, 21, 45, 80, 128, 0) == 2 * 75600 * 40 * 128 * 2
+    assert L.vdx_rope3d_workspace_bytes(2, 40, 21, 45, 80, 128, 1) == 2 * 75600 * 40 * 128 * 4
+    assert L.vdx_rope3d_workspace_bytes(0, 40, 21, 45, 80, 128, 0) == 0
 
 
 def test_ex_rejects_bad_options(L):
-    opt = _binding.AttnOptions(7, None, 0)
+    opt = _binding.AttnOptions(7, 0, None, 0)
     r = L.vdx_rope3d_attn_ex(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + (1 << 32)),
                              ctypes.c_void_p(FAKE + (2 << 32)), ctypes.c_void_p(FAKE + (3 << 32)),
                              None, 1, 2, 2, 3, 4, 128, 0, 0, 0, 10000.0, 0.0, ctypes.byref(opt), None)
     assert r == _binding.VDX_ERR_ARG and "k_rope" in L.vdx_last_error().decode()
+    opt = _binding.AttnOptions(_binding.K_ROPE_FUSED, _binding.QK_SPLIT, None, 0)
+    r = L.vdx_rope3d_attn_ex(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + (1 << 32)),
+                             ctypes.c_void_p(FAKE + (2 << 32)), ctypes.c_void_p(FAKE + (3 << 32)),
+                             None, 1, 2, 2, 3, 4, 128, 0, 0, 0, 10000.0, 0.0, ctypes.byref(opt), None)
+    assert r == _binding.VDX_ERR_UNSUPPORTED and "prepass" in L.vdx_last_error().decode()
 
 
 def test_python_binding_rejects_mismatched_grid(L):

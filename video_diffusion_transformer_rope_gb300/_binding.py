@@ -16,18 +16,19 @@ STATUS_NAMES = {0: "VDX_OK", 1: "VDX_ERR_ARG", 2: "VDX_ERR_ALIGN", 3: "VDX_ERR_U
 _p, _i, _d, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_float
 
 K_ROPE_DEFAULT, K_ROPE_PREPASS, K_ROPE_FUSED = 0, 1, 2
+QK_FP16, QK_SPLIT = 0, 1
 
 
 class AttnOptions(ctypes.Structure):
     """vdx_attn_options (include/vdx.h)."""
-    _fields_ = [("k_rope", ctypes.c_int), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_size_t)]
+    _fields_ = [("k_rope", ctypes.c_int), ("qk_precision", ctypes.c_int),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 # name -> (restype, argtypes); mirrors include/vdx.h
 SIGNATURES = {
     "vdx_rope3d_attn": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f, _p]),
     "vdx_rope3d_attn_ex": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f,
                                 ctypes.POINTER(AttnOptions), _p]),
-    "vdx_rope3d_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i]),
+    "vdx_rope3d_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i, _i]),
     "vdx_rope3d_attn_f32": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f, _p]),
     "vdx_rope3d_attn_noalloc": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f, _p]),
     "vdx_sync_check": (_i, [_p]),
@@ -74,13 +75,15 @@ def _stream_handle(stream):
 
 
 def rope3d_attn(q, k, v, grid, sections=(0, 0, 0), theta=10000.0, scale=0.0, out=None,
-                lse=None, return_lse=True, stream=None, k_rope=K_ROPE_DEFAULT, workspace=None):
+                lse=None, return_lse=True, stream=None, k_rope=K_ROPE_DEFAULT, workspace=None,
+                qk_precision=QK_FP16):
     """3D-RoPE attention of CUDA tensors q, k, v laid out [B, N, H, d] (bf16 with d = 128, or
     float32 with d = 64/128).  grid = (T, Hgrid, Wgrid) with N = T*Hgrid*Wgrid.
 
     bf16 only: k_rope selects how K is rotated (K_ROPE_PREPASS, the default, or K_ROPE_FUSED);
-    workspace is an optional CUDA tensor of at least workspace_bytes(...) bytes for the
-    prepass (None: the library's own per-device buffer).
+    qk_precision QK_SPLIT keeps hi + lo fp16 parts of every rotated value (three products,
+    for logits in the hundreds); workspace is an optional CUDA tensor of at least
+    workspace_bytes(...) bytes for the prepass (None: the library's own per-device buffer).
 
     Returns (out [B, N, H, d] in the input dtype, lse [B, H, N] float32 or None).  Enqueued on
     `stream` (default: torch's current stream); call sync_check() to surface device errors.
@@ -105,10 +108,11 @@ def rope3d_attn(q, k, v, grid, sections=(0, 0, 0), theta=10000.0, scale=0.0, out
             ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr() if lse is not None else 0),
             B, H, T, Hg, Wg, d, st, sh, sw, float(theta), float(scale), _stream_handle(stream))
     if q.dtype == torch.bfloat16:
-        if k_rope == K_ROPE_DEFAULT and workspace is None:
+        if k_rope == K_ROPE_DEFAULT and workspace is None and qk_precision == QK_FP16:
             _check(lib().vdx_rope3d_attn(*args))
         else:
-            opt = AttnOptions(int(k_rope), ctypes.c_void_p(workspace.data_ptr() if workspace is not None else 0),
+            opt = AttnOptions(int(k_rope), int(qk_precision),
+                              ctypes.c_void_p(workspace.data_ptr() if workspace is not None else 0),
                               workspace.numel() * workspace.element_size() if workspace is not None else 0)
             _check(lib().vdx_rope3d_attn_ex(*args[:-1], ctypes.byref(opt), args[-1]))
     elif q.dtype == torch.float32:
@@ -118,10 +122,10 @@ def rope3d_attn(q, k, v, grid, sections=(0, 0, 0), theta=10000.0, scale=0.0, out
     return out, lse
 
 
-def workspace_bytes(B, H, grid, d=128):
+def workspace_bytes(B, H, grid, d=128, qk_precision=QK_FP16):
     """Bytes of scratch the K prepass needs (vdx_rope3d_workspace_bytes)."""
     T, Hg, Wg = (int(x) for x in grid)
-    return lib().vdx_rope3d_workspace_bytes(B, H, T, Hg, Wg, d)
+    return lib().vdx_rope3d_workspace_bytes(B, H, T, Hg, Wg, d, qk_precision)
 
 
 def sync_check(stream=None):

@@ -22,6 +22,9 @@ class Workload:
     theta: float = 10000.0
     seed: int = 0
     stress: bool = False   # outlier channels/tokens (large-logit softmax stress)
+    # QK operand precision the workload is run with: "fp16" (default) or "split" (hi + lo fp16
+    # parts, for logits in the hundreds, where 11 significant bits leave lse errors of ~0.1)
+    qk: str = "fp16"
 
     @property
     def N(self) -> int:
@@ -51,7 +54,7 @@ WAN14B_480P = Workload("wan14b_480p", B=2, H=40, d=128, T=21, Hg=30, Wg=52, dtyp
 WAN14B_720P = Workload("wan14b_720p", B=2, H=40, d=128, T=21, Hg=45, Wg=80, dtype="bf16",
                        sections=(44, 42, 42), seed=3)
 LONG_STRESS = Workload("long_clip_stress", B=1, H=40, d=128, T=31, Hg=45, Wg=80, dtype="bf16",
-                       sections=(44, 42, 42), seed=4, stress=True)
+                       sections=(44, 42, 42), seed=4, stress=True, qk="split")
 
 ALL = (TINY_F32, WAN13B_480P, WAN14B_480P, WAN14B_720P, LONG_STRESS)
 BY_NAME = {w.name: w for w in ALL}

@@ -22,6 +22,10 @@
 // workspace and the attention kernel streams that, so no K rotation sits in the hot loop.
 // Fused: TMA brings raw bf16 K and WG2 rotates each K tile in shared memory before the MMA
 // reads it (every CTA of a head repeats this for every K tile).
+// Split (precise): as prepass, but every rotated Q/K value x is kept as two fp16 numbers,
+// hi = fp16(x) and lo = fp16(x - hi), and S = Qhi Khi^T + Qhi Klo^T + Qlo Khi^T (about 22
+// significant bits per operand instead of 11) for inputs whose logits reach the hundreds.
+// Three QK products and one-stage K/V rings (shared memory holds Q hi+lo and K hi+lo).
 //
 // TMEM (512 columns x 128 lanes, fp32): S0 [0,128)  S1 [128,256)  O0 [256,384)  O1 [384,512).
 // P_i (bf16, two per column) overwrites the first 64 columns of S_i and is the A operand of
@@ -60,20 +64,27 @@ constexpr int kTmemCols = 512;
 constexpr int kMaxStages = 3;
 constexpr int kMaxDynSmem = 232448;      // sm_100-family opt-in limit per CTA
 
-// Registers per thread after the split (sum over the 4 warpgroups = 512 x 128 at launch).
-constexpr uint32_t kRegsSoftmax = 192;
-constexpr uint32_t kRegsRope = 56;
-constexpr uint32_t kRegsCtl = 72;
-static_assert(2 * kRegsSoftmax + kRegsRope + kRegsCtl <= 4 * 128, "register split over budget");
 
-template <bool kFusedK>
+enum : int { kModePrepass = 0, kModeFused = 1, kModeSplit = 2 };
+
+template <int kMode>
 struct Layout {
-  static constexpr int kKStages = kFusedK ? 2 : 3;
-  static constexpr int kVStages = 2;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQTiles * kTileBytes;
-  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr bool kFusedK = kMode == kModeFused;
+  static constexpr bool kSplit = kMode == kModeSplit;
+  static constexpr int kKStages = kMode == kModePrepass ? 3 : (kMode == kModeFused ? 2 : 1);
+  static constexpr int kVStages = kSplit ? 1 : 2;
+  static constexpr int kKStageBytes = kSplit ? 2 * kTileBytes : kTileBytes;   // hi [+ lo]
+  static constexpr int kOffQ = 0;                                              // Q (hi) tiles
+  static constexpr int kOffQlo = kOffQ + kQTiles * kTileBytes;                 // Q lo tiles
+  static constexpr int kOffK = kOffQlo + (kSplit ? kQTiles * kTileBytes : 0);
+  static constexpr int kOffV = kOffK + kKStages * kKStageBytes;
   static constexpr int kOffTab = kOffV + kVStages * kTileBytes;
+  // Registers per thread after the role split (sum over the 4 warpgroups = 512 x 128 at
+  // launch); the split mode's MMA warp issues three QK chains and needs more.
+  static constexpr uint32_t kRegsSoftmax = kSplit ? 176 : 192;
+  static constexpr uint32_t kRegsRope = 56;
+  static constexpr uint32_t kRegsCtl = kSplit ? 104 : 72;
+  static_assert(2 * kRegsSoftmax + kRegsRope + kRegsCtl <= 4 * 128, "register split over budget");
 };
 
 // Wait sites recorded in the error word when a bounded wait gives up.
@@ -140,12 +151,12 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // Each operand is two 16 KB halves (channels 0-63, 64-127); inside a 128-byte swizzled
 // half, K step kk starts 32 bytes further on.
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
-                                         uint32_t idesc) {
+                                         uint32_t idesc, bool accumulate = false) {
 #pragma unroll
   for (int kk = 0; kk < kD / 16; ++kk) {
     const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
     mma_ss(d_tmem, smem_desc_sw128(a_smem + off, 16, 1024),
-           smem_desc_sw128(b_smem + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+           smem_desc_sw128(b_smem + off, 16, 1024), idesc, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -189,9 +200,12 @@ __device__ __forceinline__ RopeLane make_rope_lane(int c16, int half_t, int half
 
 // Rotate the 4 pairs of one 16-byte chunk (bf16 in) of a token at grid position (pt,ph,pw);
 // returns the fp16 result and folds |rotated| into amax.
+template <bool kLo>
 __device__ __forceinline__ uint4 rotate_chunk(uint4 x, const RopeLane& L, int pt, int ph, int pw,
-                                              const float2* __restrict__ tab, float& amax) {
+                                              const float2* __restrict__ tab, float& amax,
+                                              uint4* lo_out = nullptr) {
   uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint32_t wl[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const int pos = L.axis[e] == 0 ? pt : (L.axis[e] == 1 ? ph : pw);
@@ -202,15 +216,22 @@ __device__ __forceinline__ uint4 rotate_chunk(uint4 x, const RopeLane& L, int pt
     const float y1 = fmaf(x0, cs.y, x1 * cs.x);
     amax = fmax3(amax, fabsf(y0), fabsf(y1));
     w[e] = pack_f16x2_sat(y0, y1);
+    if (kLo) {
+      const __half2 hi = *reinterpret_cast<const __half2*>(&w[e]);
+      wl[e] = pack_f16x2_sat(y0 - __low2float(hi), y1 - __high2float(hi));
+    }
   }
+  if (kLo) *lo_out = make_uint4(wl[0], wl[1], wl[2], wl[3]);
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // Rotate one 128-row tile in place (bf16 in, fp16 out, swizzled halves).  Thread t handles
 // chunk (t & 15) of rows (t >> 4) + 8*it; the 8 threads sharing a row hit 8 distinct
 // 16-byte bank groups.
+template <bool kLo>
 __device__ __forceinline__ float rope_tile(const Params& p, const RopeLane& L, int t, uint8_t* tile,
-                                           int n_first, const float2* __restrict__ tab) {
+                                           int n_first, const float2* __restrict__ tab,
+                                           uint8_t* lo_tile = nullptr) {
   float amax = 0.f;
   const int c16 = t & 15;
   const int rsub = t >> 4;
@@ -225,7 +246,8 @@ __device__ __forceinline__ float rope_tile(const Params& p, const RopeLane& L, i
   for (int it = 0; it < kBM / 8; ++it) {
     if (n >= p.N) break;
     uint4* ptr = reinterpret_cast<uint4*>(tile + chunk_off + it * 1024);
-    *ptr = rotate_chunk(*ptr, L, pt, ph, pw, tab, amax);
+    *ptr = rotate_chunk<kLo>(*ptr, L, pt, ph, pw, tab, amax,
+                             kLo ? reinterpret_cast<uint4*>(lo_tile + chunk_off + it * 1024) : nullptr);
     n += 8;
     pw += 8;
     while (pw >= p.Wg) { pw -= p.Wg; ++ph; }
@@ -234,11 +256,14 @@ __device__ __forceinline__ float rope_tile(const Params& p, const RopeLane& L, i
   return amax;
 }
 
-template <bool kFusedK>
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const Params p) {
-  using Lo = Layout<kFusedK>;
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_klo,
+               const Params p) {
+  using Lo = Layout<kMode>;
+  constexpr bool kFusedK = Lo::kFusedK;
+  constexpr bool kSplit = Lo::kSplit;
   constexpr int kKStages = Lo::kKStages;
   constexpr int kVStages = Lo::kVStages;
   extern __shared__ uint8_t smem_raw[];
@@ -296,12 +321,13 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   volatile int* abort_flag = &ctl->abort_flag;
 
   if (warp >= 12) {
-    regs_decrease<kRegsCtl>();
+    regs_decrease<Lo::kRegsCtl>();
     if (warp == 12 && lane == 0) {
       // ---------------------------------------------------------- TMA producer
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
+      if (kSplit) tma_prefetch_desc(&tm_klo);
       for (int i = 0; i < kQTiles; ++i) {
         const uint32_t bar = smem_addr(&ctl->q_full[i]);
         mbar_arrive_expect_tx(bar, kTileBytes);
@@ -316,10 +342,14 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           break;
         {
           const uint32_t bar = smem_addr(&ctl->k_full[ks]);
-          mbar_arrive_expect_tx(bar, kTileBytes);
-          const uint32_t dst = sK + ks * kTileBytes;
+          mbar_arrive_expect_tx(bar, Lo::kKStageBytes);
+          const uint32_t dst = sK + ks * Lo::kKStageBytes;
           tma_load_4d(dst, &tm_k, bar, 0, h, j * kBN, b);
           tma_load_4d(dst + kHalfBytes, &tm_k, bar, 64, h, j * kBN, b);
+          if (kSplit) {
+            tma_load_4d(dst + kTileBytes, &tm_klo, bar, 0, h, j * kBN, b);
+            tma_load_4d(dst + kTileBytes + kHalfBytes, &tm_klo, bar, 64, h, j * kBN, b);
+          }
           k_issued = j + 1;
         }
         const int vs = j % kVStages, vu = j / kVStages;
@@ -358,8 +388,13 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!(ok = mbar_wait(kbar, (j / kKStages) & 1, abort_flag, kFusedK ? kSiteKReady : kSiteKFull)))
           break;
         tc_fence_after_sync();
-        const uint32_t kt = sK + ks * kTileBytes;
+        const uint32_t kt = sK + ks * Lo::kKStageBytes;
+        const uint32_t sQlo = smem_addr(smem + Lo::kOffQlo);
         issue_qk(tS0, sQ, kt, kIdQK);
+        if (kSplit) {
+          issue_qk(tS0, sQ, kt + kTileBytes, kIdQK, true);     // Qhi Klo
+          issue_qk(tS0, sQlo, kt, kIdQK, true);                // Qlo Khi
+        }
         mma_commit(smem_addr(&ctl->s_full[0]));
         if (j > 0) {
           if (!(ok = mbar_wait(smem_addr(&ctl->p_ready[1]), (j - 1) & 1, abort_flag, kSitePReady)))
@@ -370,6 +405,10 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           mma_commit(smem_addr(&ctl->v_empty[pvs]));
         }
         issue_qk(tS1, sQ + kTileBytes, kt, kIdQK);
+        if (kSplit) {
+          issue_qk(tS1, sQ + kTileBytes, kt + kTileBytes, kIdQK, true);
+          issue_qk(tS1, sQlo + kTileBytes, kt, kIdQK, true);
+        }
         mma_commit(smem_addr(&ctl->s_full[1]));
         mma_commit(smem_addr(&ctl->k_empty[ks]));
         const int vs = j % kVStages;
@@ -392,7 +431,7 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __syncwarp();
   } else if (warp >= 8) {
     // ------------------------------------------------------------ RoPE on Q (and K tiles)
-    regs_decrease<kRegsRope>();
+    regs_decrease<Lo::kRegsRope>();
     const int t = tid - 256;
     const float2* tab = (kFusedK && p.table_in_smem) ? tab_s : p.table;
     const RopeLane L = make_rope_lane(t & 15, p.half_t, p.half_h, p.half_w, p.off_h, p.off_w);
@@ -400,7 +439,8 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     float amax = 0.f;
     for (int i = 0; i < kQTiles && ok; ++i) {
       if (!(ok = mbar_wait(smem_addr(&ctl->q_full[i]), 0, abort_flag, kSiteQFull))) break;
-      amax = fmaxf(amax, rope_tile(p, L, t, smem + Lo::kOffQ + i * kTileBytes, q0 + i * kBM, tab));
+      amax = fmaxf(amax, rope_tile<kSplit>(p, L, t, smem + Lo::kOffQ + i * kTileBytes, q0 + i * kBM,
+                                           tab, smem + Lo::kOffQlo + i * kTileBytes));
       fence_proxy_async_smem();
       mbar_arrive(smem_addr(&ctl->q_ready[i]));
     }
@@ -409,7 +449,7 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int ks = j % kKStages;
         if (!(ok = mbar_wait(smem_addr(&ctl->k_full[ks]), (j / kKStages) & 1, abort_flag, kSiteKFull)))
           break;
-        amax = fmaxf(amax, rope_tile(p, L, t, smem + Lo::kOffK + ks * kTileBytes, j * kBN, tab));
+        amax = fmaxf(amax, rope_tile<false>(p, L, t, smem + Lo::kOffK + ks * Lo::kKStageBytes, j * kBN, tab));
         fence_proxy_async_smem();
         mbar_arrive(smem_addr(&ctl->k_ready[ks]));
       }
@@ -417,7 +457,7 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (!(amax <= 65504.f)) atomicOr(&g_error_word, 2u);
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    regs_increase<kRegsSoftmax>();
+    regs_increase<Lo::kRegsSoftmax>();
     const int qi = warp >> 2;
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_bits = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -537,9 +577,11 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   }
 }
 
-// K prepass: rotate every token of K once (bf16 in, fp16 out, same [B, N, H, d] layout).
+// K prepass: rotate every token of K once (bf16 in, fp16 out, same [B, N, H, d] layout; with
+// kLo the fp16 remainders follow as a second [B, N, H, d] tensor).
 // One thread per 16-byte chunk; the grid stride is a multiple of 16 chunks, so each thread
 // keeps one chunk column (and its four rotary pairs) throughout.
+template <bool kLo>
 __global__ void __launch_bounds__(256)
 rope3d_k_prepass(const uint4* __restrict__ k, uint4* __restrict__ kr, const Params p,
                  uint32_t n_chunks) {
@@ -556,7 +598,7 @@ rope3d_k_prepass(const uint4* __restrict__ k, uint4* __restrict__ kr, const Para
     const int ph = rem / p.Wg;
     const int pw = rem - ph * p.Wg;
     const uint4 x = __ldg(k + c);
-    kr[c] = rotate_chunk(x, L, pt, ph, pw, p.table, amax);
+    kr[c] = rotate_chunk<kLo>(x, L, pt, ph, pw, p.table, amax, kLo ? kr + n_chunks + c : nullptr);
   }
   if (!(amax <= 65504.f)) atomicOr(&g_error_word, 2u);
 }
@@ -589,10 +631,11 @@ CUresult encode_bhnd(EncodeTiledFn encode, CUtensorMap* map, const void* base,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <bool kFusedK>
+template <int kMode>
 cudaError_t launch_attn(const Problem& pr, Params p, const CUtensorMap* maps, cudaStream_t stream,
                         const char** what) {
-  using Lo = Layout<kFusedK>;
+  using Lo = Layout<kMode>;
+  constexpr bool kFusedK = Lo::kFusedK;
   const int tab_bytes = ((pr.table_entries * 8) + 15) & ~15;
   const int ctl_bytes = (static_cast<int>(sizeof(Ctl)) + 15) & ~15;
   int smem = Lo::kOffTab + tab_bytes + ctl_bytes + 1024;
@@ -604,7 +647,7 @@ cudaError_t launch_attn(const Problem& pr, Params p, const CUtensorMap* maps, cu
     p.ctl_off = Lo::kOffTab;
     smem = Lo::kOffTab + ctl_bytes + 1024;
   }
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_sm103<kFusedK>,
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_sm103<kMode>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) {
     *what = "cudaFuncSetAttribute(max dynamic shared memory) failed";
@@ -615,7 +658,8 @@ cudaError_t launch_attn(const Problem& pr, Params p, const CUtensorMap* maps, cu
     *what = "grid too large";
     return cudaErrorInvalidValue;
   }
-  attn_fwd_sm103<kFusedK><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(maps[0], maps[1], maps[2], p);
+  attn_fwd_sm103<kMode><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(maps[0], maps[1], maps[2],
+                                                                              maps[3], p);
   e = cudaGetLastError();
   if (e != cudaSuccess) *what = "attention kernel launch failed";
   return e;
@@ -630,20 +674,23 @@ cudaError_t read_and_clear_error_word_sm103(unsigned int* word) {
   return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
 }
 
-size_t k_prepass_workspace_bytes(const Problem& pr) {
-  return static_cast<size_t>(pr.B) * pr.N * pr.H * kD * 2;
+size_t k_prepass_workspace_bytes(const Problem& pr, bool split) {
+  return static_cast<size_t>(pr.B) * pr.N * pr.H * kD * 2 * (split ? 2 : 1);
 }
 
-cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, bool fused_k,
+cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, KMode mode,
                                    void* workspace, cudaStream_t stream, const char** what) {
   *what = nullptr;
   Params p;
   fill_params(pr, &p);
-  CUtensorMap maps[3];
+  CUtensorMap maps[4];
+  const bool fused = mode == KMode::kFused;
+  const bool split = mode == KMode::kSplit;
   const void* kbase = pr.k;
-  if (!fused_k) {
-    const size_t chunks = k_prepass_workspace_bytes(pr) / 16;
-    if (chunks >= 0x80000000ull) {
+  const void* klo = pr.k;
+  if (!fused) {
+    const size_t chunks = k_prepass_workspace_bytes(pr, false) / 16;
+    if (chunks >= 0x40000000ull) {
       *what = "K prepass: tensor too large";
       return cudaErrorInvalidValue;
     }
@@ -653,25 +700,33 @@ cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, bool
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long want = (static_cast<long long>(chunks) + 255) / 256;
     const unsigned blocks = static_cast<unsigned>(std::min<long long>(want, static_cast<long long>(sms) * 8));
-    rope3d_k_prepass<<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(pr.k),
-                                                  static_cast<uint4*>(workspace), p,
-                                                  static_cast<uint32_t>(chunks));
+    if (split)
+      rope3d_k_prepass<true><<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(pr.k),
+                                                          static_cast<uint4*>(workspace), p,
+                                                          static_cast<uint32_t>(chunks));
+    else
+      rope3d_k_prepass<false><<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(pr.k),
+                                                           static_cast<uint4*>(workspace), p,
+                                                           static_cast<uint32_t>(chunks));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
       *what = "K prepass launch failed";
       return e;
     }
     kbase = workspace;
+    klo = static_cast<const uint8_t*>(workspace) + k_prepass_workspace_bytes(pr, false);
   }
+  const CUtensorMapDataType kdt = fused ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   if (encode_bhnd(encode, &maps[0], pr.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr) != CUDA_SUCCESS ||
-      encode_bhnd(encode, &maps[1], kbase,
-                  fused_k ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, pr) != CUDA_SUCCESS ||
-      encode_bhnd(encode, &maps[2], pr.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr) != CUDA_SUCCESS) {
+      encode_bhnd(encode, &maps[1], kbase, kdt, pr) != CUDA_SUCCESS ||
+      encode_bhnd(encode, &maps[2], pr.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr) != CUDA_SUCCESS ||
+      encode_bhnd(encode, &maps[3], split ? klo : kbase, kdt, pr) != CUDA_SUCCESS) {
     *what = "cuTensorMapEncodeTiled failed";
     return cudaErrorInvalidValue;
   }
-  return fused_k ? launch_attn<true>(pr, p, maps, stream, what)
-                 : launch_attn<false>(pr, p, maps, stream, what);
+  if (fused) return launch_attn<kModeFused>(pr, p, maps, stream, what);
+  if (split) return launch_attn<kModeSplit>(pr, p, maps, stream, what);
+  return launch_attn<kModePrepass>(pr, p, maps, stream, what);
 }
 
 }  // namespace vdx

@@ -202,14 +202,20 @@ vdx_status vdx_rope3d_attn_ex(const void* q, const void* k, const void* v, void*
   const int mode = opt ? opt->k_rope : VDX_K_ROPE_DEFAULT;
   if (mode != VDX_K_ROPE_DEFAULT && mode != VDX_K_ROPE_PREPASS && mode != VDX_K_ROPE_FUSED)
     return fail(VDX_ERR_ARG, "unknown k_rope mode %d", mode);
+  const int prec = opt ? opt->qk_precision : VDX_QK_FP16;
+  if (prec != VDX_QK_FP16 && prec != VDX_QK_SPLIT)
+    return fail(VDX_ERR_ARG, "unknown qk_precision %d", prec);
   const bool fused = mode == VDX_K_ROPE_FUSED;
+  const bool split = prec == VDX_QK_SPLIT;
+  if (fused && split)
+    return fail(VDX_ERR_UNSUPPORTED, "VDX_QK_SPLIT needs the K prepass (k_rope = VDX_K_ROPE_PREPASS)");
   vdx::Problem p{};
   vdx_status s = prepare(q, k, v, out, lse, B, H, T, Hgrid, Wgrid, d, sec_t, sec_h, sec_w, theta,
                          scale, 2, &p);
   if (s != VDX_OK) return s;
   void* ws = nullptr;
   if (!fused) {
-    const size_t need = vdx::k_prepass_workspace_bytes(p);
+    const size_t need = vdx::k_prepass_workspace_bytes(p, split);
     if (opt && opt->workspace) {
       if (opt->workspace_bytes < need)
         return fail(VDX_ERR_ARG, "workspace of %zu bytes is smaller than the %zu needed",
@@ -228,7 +234,8 @@ vdx_status vdx_rope3d_attn_ex(const void* q, const void* k, const void* v, void*
   vdx::EncodeTiledFn enc = nullptr;
   if ((s = get_encode(&enc)) != VDX_OK) return s;
   const char* what = nullptr;
-  cudaError_t e = vdx::launch_attn_bf16_sm103(p, enc, fused, ws, static_cast<cudaStream_t>(stream), &what);
+  const vdx::KMode km = fused ? vdx::KMode::kFused : (split ? vdx::KMode::kSplit : vdx::KMode::kPrepass);
+  cudaError_t e = vdx::launch_attn_bf16_sm103(p, enc, km, ws, static_cast<cudaStream_t>(stream), &what);
   if (e != cudaSuccess)
     return fail(VDX_ERR_CUDA, "%s: %s", what ? what : "launch", cudaGetErrorString(e));
   return VDX_OK;
@@ -241,9 +248,10 @@ vdx_status vdx_rope3d_attn(const void* q, const void* k, const void* v, void* ou
                             theta, scale, nullptr, stream);
 }
 
-size_t vdx_rope3d_workspace_bytes(int B, int H, int T, int Hgrid, int Wgrid, int d) {
+size_t vdx_rope3d_workspace_bytes(int B, int H, int T, int Hgrid, int Wgrid, int d,
+                                  int qk_precision) {
   if (B < 1 || H < 1 || T < 1 || Hgrid < 1 || Wgrid < 1 || d < 1) return 0;
-  return static_cast<size_t>(B) * T * Hgrid * Wgrid * H * d * 2;
+  return static_cast<size_t>(B) * T * Hgrid * Wgrid * H * d * 2 * (qk_precision == VDX_QK_SPLIT ? 2 : 1);
 }
 
 vdx_status vdx_rope3d_attn_f32(const float* q, const float* k, const float* v, float* out,

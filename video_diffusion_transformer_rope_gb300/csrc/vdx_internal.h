@@ -29,12 +29,17 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-// fused_k = false: K is first rotated once into `workspace` (fp16, [B, N, H, d], at least
-// k_prepass_workspace_bytes(p) bytes, 16-byte aligned) by a prepass kernel on the same stream.
-// fused_k = true: every CTA rotates its K tiles in shared memory; `workspace` is unused.
-cudaError_t launch_attn_bf16_sm103(const Problem& p, EncodeTiledFn encode, bool fused_k,
+// How K is rotated and how precise the QK^T operands are.
+//   kPrepass: K is first rotated once into `workspace` (fp16 [B, N, H, d]) by a prepass kernel
+//             on the same stream; fp16 QK operands.
+//   kFused:   every CTA rotates its K tiles in shared memory; `workspace` is unused.
+//   kSplit:   as kPrepass, with every rotated value split into fp16 hi + lo (workspace holds
+//             both) and three QK products.
+enum class KMode { kPrepass, kFused, kSplit };
+cudaError_t launch_attn_bf16_sm103(const Problem& p, EncodeTiledFn encode, KMode mode,
                                    void* workspace, cudaStream_t stream, const char** what);
-size_t k_prepass_workspace_bytes(const Problem& p);
+// Workspace bytes for kPrepass (split = false) or kSplit (split = true).
+size_t k_prepass_workspace_bytes(const Problem& p, bool split);
 
 // Read the tensor-core kernel's device error word (synchronous) and reset it to 0.
 cudaError_t read_and_clear_error_word_sm103(unsigned int* word);
