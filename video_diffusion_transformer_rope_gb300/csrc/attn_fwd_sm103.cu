@@ -150,13 +150,14 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // S(tmem) = A(smem, 128 x 128, K-major) * B(smem, 128 x 128, K-major)^T in 8 steps of K=16.
 // Each operand is two 16 KB halves (channels 0-63, 64-127); inside a 128-byte swizzled
 // half, K step kk starts 32 bytes further on.
+// Called by the whole MMA warp; one elected lane issues.
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
                                          uint32_t idesc, bool accumulate = false) {
 #pragma unroll
   for (int kk = 0; kk < kD / 16; ++kk) {
     const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-    mma_ss(d_tmem, smem_desc_sw128(a_smem + off, 16, 1024),
-           smem_desc_sw128(b_smem + off, 16, 1024), idesc, (accumulate || kk > 0) ? 1u : 0u);
+    mma_ss_warp(d_tmem, smem_desc_sw128(a_smem + off, 16, 1024),
+                smem_desc_sw128(b_smem + off, 16, 1024), idesc, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -167,8 +168,8 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
                                          uint32_t idesc, bool accumulate) {
 #pragma unroll
   for (int kk = 0; kk < kBN / 16; ++kk) {
-    mma_ts(d_tmem, p_tmem + kk * 8, smem_desc_sw128(v_smem + kk * 2048, kHalfBytes, 1024), idesc,
-           (accumulate || kk > 0) ? 1u : 0u);
+    mma_ts_warp(d_tmem, p_tmem + kk * 8, smem_desc_sw128(v_smem + kk * 2048, kHalfBytes, 1024),
+                idesc, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -374,19 +375,22 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int uses = v_issued > s ? (v_issued - 1 - s) / kVStages + 1 : 0;
         if (uses > 0) drain_wait(smem_addr(&ctl->v_full[s]), (uses - 1) & 1);
       }
-    } else if (warp == 13 && lane == 0) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if (warp == 13) {
+      // ---------------------------------------------------------- MMA issuer (whole warp runs
+      // the loop so descriptor arithmetic stays warp-uniform; one elected lane issues)
       constexpr uint32_t kIdQK = idesc_f16kind_f32acc(kBM, kBN, 0, 0);   // fp16 Q', K'
       constexpr uint32_t kIdPV = idesc_f16kind_f32acc(kBM, kD, 1, 1);   // bf16 P, V (MN-major)
       const uint32_t tS0 = tmem + 0, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
       bool ok = mbar_wait(smem_addr(&ctl->q_ready[0]), 0, abort_flag, kSiteQReady) &&
                 mbar_wait(smem_addr(&ctl->q_ready[1]), 0, abort_flag, kSiteQReady);
+      ok = __all_sync(0xffffffffu, ok);
       tc_fence_after_sync();
       for (int j = 0; ok && j < nkv; ++j) {
         const int ks = j % kKStages;
         const uint32_t kbar = kFusedK ? smem_addr(&ctl->k_ready[ks]) : smem_addr(&ctl->k_full[ks]);
-        if (!(ok = mbar_wait(kbar, (j / kKStages) & 1, abort_flag, kFusedK ? kSiteKReady : kSiteKFull)))
-          break;
+        ok = __all_sync(0xffffffffu, mbar_wait(kbar, (j / kKStages) & 1, abort_flag,
+                                               kFusedK ? kSiteKReady : kSiteKFull));
+        if (!ok) break;
         tc_fence_after_sync();
         const uint32_t kt = sK + ks * Lo::kKStageBytes;
         const uint32_t sQlo = smem_addr(smem + Lo::kOffQlo);
@@ -395,37 +399,39 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           issue_qk(tS0, sQ, kt + kTileBytes, kIdQK, true);     // Qhi Klo
           issue_qk(tS0, sQlo, kt, kIdQK, true);                // Qlo Khi
         }
-        mma_commit(smem_addr(&ctl->s_full[0]));
+        mma_commit_warp(smem_addr(&ctl->s_full[0]));
         if (j > 0) {
-          if (!(ok = mbar_wait(smem_addr(&ctl->p_ready[1]), (j - 1) & 1, abort_flag, kSitePReady)))
-            break;
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->p_ready[1]), (j - 1) & 1, abort_flag,
+                                                 kSitePReady));
+          if (!ok) break;
           tc_fence_after_sync();
           const int pvs = (j - 1) % kVStages;
           issue_pv(tO1, tS1, sV + pvs * kTileBytes, kIdPV, j - 1 > 0);
-          mma_commit(smem_addr(&ctl->v_empty[pvs]));
+          mma_commit_warp(smem_addr(&ctl->v_empty[pvs]));
         }
         issue_qk(tS1, sQ + kTileBytes, kt, kIdQK);
         if (kSplit) {
           issue_qk(tS1, sQ + kTileBytes, kt + kTileBytes, kIdQK, true);
           issue_qk(tS1, sQlo + kTileBytes, kt, kIdQK, true);
         }
-        mma_commit(smem_addr(&ctl->s_full[1]));
-        mma_commit(smem_addr(&ctl->k_empty[ks]));
+        mma_commit_warp(smem_addr(&ctl->s_full[1]));
+        mma_commit_warp(smem_addr(&ctl->k_empty[ks]));
         const int vs = j % kVStages;
-        if (!(ok = mbar_wait(smem_addr(&ctl->v_full[vs]), (j / kVStages) & 1, abort_flag, kSiteVFull)))
-          break;
-        if (!(ok = mbar_wait(smem_addr(&ctl->p_ready[0]), j & 1, abort_flag, kSitePReady))) break;
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(smem_addr(&ctl->v_full[vs]), (j / kVStages) & 1, abort_flag, kSiteVFull) &&
+                        mbar_wait(smem_addr(&ctl->p_ready[0]), j & 1, abort_flag, kSitePReady));
+        if (!ok) break;
         tc_fence_after_sync();
         issue_pv(tO0, tS0, sV + vs * kTileBytes, kIdPV, j > 0);
       }
       if (ok) {
         const int jl = nkv - 1;
-        if (mbar_wait(smem_addr(&ctl->p_ready[1]), jl & 1, abort_flag, kSitePReady)) {
+        if (__all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->p_ready[1]), jl & 1, abort_flag, kSitePReady))) {
           tc_fence_after_sync();
           issue_pv(tO1, tS1, sV + (jl % kVStages) * kTileBytes, kIdPV, jl > 0);
         }
       }
-      mma_commit(smem_addr(&ctl->o_final));
+      mma_commit_warp(smem_addr(&ctl->o_final));
       drain_wait(smem_addr(&ctl->o_final), 0);
     }
     __syncwarp();
