@@ -92,8 +92,10 @@ def test_bf16_caller_workspace_matches_library_workspace():
     o2, l2 = _run(w, q, k, v)
     o3, l3 = _run(w, q, k, v, k_rope=vdx.K_ROPE_FUSED)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
-    # the two K modes round the same rotated values to fp16: identical scores and output
-    assert torch.equal(o1, o3) and torch.equal(l1, l3)
+    # the two K modes round the same rotated values to fp16 (same scores); the kernels may
+    # order their sums differently, so the outputs agree to rounding, not bit for bit
+    assert (o1.float() - o3.float()).abs().max().item() <= 2e-3
+    assert (l1 - l3).abs().max().item() <= 1e-4
     with pytest.raises(vdx.VdxError) as ei:
         vdx.rope3d_attn(q, k, v, (w.T, w.Hg, w.Wg), workspace=ws[:100])
     assert ei.value.status == 1
@@ -120,6 +122,20 @@ def test_bf16_large_logits_small():
     # why this workload uses the split mode; the output itself stays within tolerance
     mx16, mean16, lerr16 = _full_compare(w, qk_precision=vdx.QK_FP16)
     assert mx16 <= BF16_MAX and lerr16 > LSE_TOL
+
+
+def test_bf16_late_logit_jump():
+    # keys of the last tile scaled x25: for most rows the running maximum jumps by far more
+    # than the kernel's in-range margin on tile 3, which takes its exact reload route.  Logits
+    # this large need the split operands (fp16 alone leaves ~3e-2 here, as on the stress set).
+    w = dataclasses.replace(configs.WAN13B_480P, B=1, H=2, T=4, Hg=8, Wg=16, seed=27, qk="split")
+    q, k, v = synth.make_qkv(w)
+    k = k.float()
+    k[:, 400:410] *= 25.0
+    k = k.to(torch.bfloat16)
+    dev = tuple(t.cuda() for t in (q, k, v))
+    mx, mean, lerr = _full_compare(w, dev)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
 
 
 def test_bf16_deterministic_and_guard_bands():
