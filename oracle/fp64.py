@@ -161,3 +161,82 @@ def rope3d_attention_rows(q, k, v, grid, rows, sections=None, theta=10000.0, sca
             o[i] = oo[j]
             lse[i] = ll[j]
     return o, lse
+
+
+# ---------------------------------------------------------------------------------------------
+# Block-sparse variant (ScalingAttention's "bit-wise block-sparse kernel", named on the first
+# page; the block masks themselves come from trained weights there, synthetic here).
+#
+# Definition: the keys are cut into blocks of `kblock` consecutive tokens and the queries into
+# blocks of `qblock` consecutive tokens; query n attends only to the keys of the blocks that
+# the mask marks for its query block.  A query whose mask row is empty has no keys: its
+# output is 0 and its lse is -inf.  mask: bool array [B, H, n_qblocks, n_kblocks] (or
+# [n_qblocks, n_kblocks], shared by every (b, h)).
+
+def block_key_mask(mask_qk, N, qblock, kblock):
+    """Expand a [n_qblocks, n_kblocks] block mask to a [N, N] bool matrix (query, key)."""
+    qb = np.arange(N) // qblock
+    kb = np.arange(N) // kblock
+    return np.asarray(mask_qk, dtype=bool)[qb[:, None], kb[None, :]]
+
+
+def attention_rows_masked(qr, kr, v, scale, allowed):
+    """attention_rows restricted to allowed[r, m] keys; rows with no key give o = 0, lse = -inf."""
+    s = scale * (qr @ kr.T)
+    s = np.where(allowed, s, -np.inf)
+    m = s.max(axis=1, keepdims=True)
+    empty = ~np.isfinite(m[:, 0])
+    m = np.where(np.isfinite(m), m, 0.0)
+    p = np.exp(s - m)
+    l = p.sum(axis=1, keepdims=True)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        o = np.where(empty[:, None], 0.0, (p @ v) / np.where(l > 0, l, 1.0))
+        lse = np.where(empty, -np.inf, (m + np.log(np.where(l > 0, l, 1.0)))[:, 0])
+    return o, lse
+
+
+def rope3d_attention_blocksparse(q, k, v, grid, mask, qblock=256, kblock=128, sections=None,
+                                 theta=10000.0, scale=None):
+    """Block-sparse oracle: out [B, N, H, d], lse [B, H, N] (fp64)."""
+    q, k, v = _to64(q), _to64(k), _to64(v)
+    B, N, H, d = q.shape
+    sections = tuple(sections) if sections else default_sections(d)
+    scale = d ** -0.5 if scale is None else scale
+    mask = np.asarray(mask, dtype=bool)
+    qr = rope3d(q, grid, sections, theta)
+    kr = rope3d(k, grid, sections, theta)
+    vv = v.transpose(0, 2, 1, 3)
+    out = np.empty((B, H, N, d))
+    lse = np.empty((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            mk = mask if mask.ndim == 2 else mask[b, h]
+            allowed = block_key_mask(mk, N, qblock, kblock)
+            out[b, h], lse[b, h] = attention_rows_masked(qr[b, h], kr[b, h], vv[b, h], scale, allowed)
+    return out.transpose(0, 2, 1, 3), lse
+
+
+# ---------------------------------------------------------------------------------------------
+# Windowed 3D attention (the windowed-attention primitive of the vidax page, §2 "3D RoPE, 3D
+# VAEs, and flash attention"), at block granularity: query block Qb attends to key block Kb
+# when some query of Qb and some key of Kb lie within (wt, wh, ww) of each other on every
+# grid axis (|dt| <= wt, |dh| <= wh, |dw| <= ww).  Expressed as a block mask for the
+# block-sparse definition above.
+
+def window_block_mask(grid, window, qblock=256, kblock=128):
+    T, Hg, Wg = grid
+    wt, wh, ww = window
+    N = T * Hg * Wg
+    t, h, w = token_positions(T, Hg, Wg)
+    nq = (N + qblock - 1) // qblock
+    nk = (N + kblock - 1) // kblock
+    mask = np.zeros((nq, nk), dtype=bool)
+    for qb in range(nq):
+        qs = slice(qb * qblock, min(N, (qb + 1) * qblock))
+        for kb in range(nk):
+            ks = slice(kb * kblock, min(N, (kb + 1) * kblock))
+            near = ((np.abs(t[qs][:, None] - t[ks][None, :]) <= wt) &
+                    (np.abs(h[qs][:, None] - h[ks][None, :]) <= wh) &
+                    (np.abs(w[qs][:, None] - w[ks][None, :]) <= ww))
+            mask[qb, kb] = bool(near.any())
+    return mask

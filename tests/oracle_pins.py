@@ -260,4 +260,83 @@ def pin_rows_match_full(O):
     assert np.allclose(o_t, o, atol=1e-15) and np.allclose(l_t, l, atol=1e-15)
 
 
+def _rotated(O, B, N, H, d, grid, seed):
+    rng = _rng(seed)
+    q, k, v = (rng.standard_normal((B, N, H, d)) for _ in range(3))
+    return q, k, v, O.rope3d(q, grid, (24, 20, 20), 10000.0), O.rope3d(k, grid, (24, 20, 20), 10000.0)
+
+
+def pin_blocksparse_all_blocks_is_dense(O):
+    """A mask with every block set is the dense oracle, bit for bit."""
+    B, H, d, grid = 1, 2, 64, (2, 5, 60)
+    N = 600
+    q, k, v, _, _ = _rotated(O, B, N, H, d, grid, 13)
+    dense_o, dense_l = O.rope3d_attention(q, k, v, grid)
+    mask = np.ones((3, 5), dtype=bool)
+    o, l = O.rope3d_attention_blocksparse(q, k, v, grid, mask)
+    assert np.array_equal(o, dense_o) and np.array_equal(l, dense_l)
+
+
+def pin_blocksparse_vs_torch_masked(O):
+    """Random block masks (every query block keeps at least one key block) equal torch's fp64
+    attention with a boolean attn_mask built from the block structure by this test."""
+    B, H, d, grid = 2, 2, 64, (3, 4, 50)
+    N = 600
+    q, k, v, qr, kr = _rotated(O, B, N, H, d, grid, 14)
+    rng = _rng(15)
+    nq, nk = (N + 255) // 256, (N + 127) // 128
+    mask = rng.random((B, H, nq, nk)) < 0.4
+    mask[..., 0, 2] = True
+    mask[..., 1, 0] = True
+    mask[..., 2, 4] = True
+    o, l = O.rope3d_attention_blocksparse(q, k, v, grid, mask)
+    for b in range(B):
+        for h in range(H):
+            allowed = np.zeros((N, N), dtype=bool)
+            for n in range(0, N, 8):                       # rows in steps (same block rows)
+                for m in range(N):
+                    allowed[n:n + 8, m] = mask[b, h, n // 256, m // 128]
+            tq = torch.from_numpy(np.ascontiguousarray(qr[b, h]))[None]
+            tk = torch.from_numpy(np.ascontiguousarray(kr[b, h]))[None]
+            tv = torch.from_numpy(np.ascontiguousarray(v[b, :, h]))[None]
+            ta = torch.from_numpy(allowed)[None]
+            ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=ta)[0].numpy()
+            sc = (tq[0] @ tk[0].T) * d ** -0.5
+            ref_l = torch.logsumexp(sc.masked_fill(~ta[0], float("-inf")), dim=-1).numpy()
+            assert np.max(np.abs(o[b, :, h] - ref)) < 1e-12
+            assert np.max(np.abs(l[b, h] - ref_l)) < 1e-12
+
+
+def pin_blocksparse_single_block_and_empty(O):
+    """One key block: attention over exactly those (rotated) keys; no block: o = 0, lse = -inf."""
+    B, H, d, grid = 1, 1, 64, (1, 6, 50)
+    N = 300
+    q, k, v, qr, kr = _rotated(O, B, N, H, d, grid, 16)
+    mask = np.zeros((2, 3), dtype=bool)
+    mask[0, 1] = True                                   # query rows 0-255 see keys 128-255
+    o, l = O.rope3d_attention_blocksparse(q, k, v, grid, mask)
+    s = (qr[0, 0, :256] @ kr[0, 0, 128:256].T) * d ** -0.5
+    ref_l = np.log(np.exp(s - s.max(1, keepdims=True)).sum(1)) + s.max(1)
+    ref_o = np.exp(s - ref_l[:, None]) @ v[0, 128:256, 0]
+    assert np.max(np.abs(o[0, :256, 0] - ref_o)) < 1e-12 and np.max(np.abs(l[0, 0, :256] - ref_l)) < 1e-12
+    assert np.all(o[0, 256:, 0] == 0.0) and np.all(np.isneginf(l[0, 0, 256:]))
+
+
+def pin_window_block_mask_brute_force(O):
+    """Window block mask against a pair-by-pair scan written out here."""
+    grid, window = (3, 7, 20), (1, 2, 3)
+    T, Hg, Wg = grid
+    N = T * Hg * Wg
+    mask = O.window_block_mask(grid, window)
+    ref = np.zeros(((N + 255) // 256, (N + 127) // 128), dtype=bool)
+    for a in range(N):
+        ta, ha, wa = a // (Hg * Wg), (a // Wg) % Hg, a % Wg
+        for c in range(N):
+            tc, hc, wc = c // (Hg * Wg), (c // Wg) % Hg, c % Wg
+            if abs(ta - tc) <= 1 and abs(ha - hc) <= 2 and abs(wa - wc) <= 3:
+                ref[a // 256, c // 128] = True
+    assert np.array_equal(mask, ref)
+    assert O.window_block_mask(grid, (T, Hg, Wg)).all()
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -11,7 +11,8 @@ from oracle_pins import ALL_PINS
 
 _orig = {name: getattr(O, name) for name in
          ("rope_frequencies", "token_positions", "rope3d_angles", "apply_rotary",
-          "attention_rows", "rope3d", "default_sections")}
+          "attention_rows", "rope3d", "default_sections", "block_key_mask",
+          "attention_rows_masked", "window_block_mask")}
 
 
 def _freq_no_two(S, theta):            # dropped factor 2 in the exponent
@@ -94,7 +95,28 @@ def _sections_thirds(d):
     return (d // 3 + d % 3, d // 3, d // 3)
 
 
+def _mask_blocks_swapped(mask_qk, N, qblock, kblock):     # query/key block sizes swapped
+    return _orig["block_key_mask"](mask_qk, N, kblock, qblock)
+
+
+def _mask_ignored(mask_qk, N, qblock, kblock):             # mask not applied
+    return np.ones((N, N), dtype=bool)
+
+
+def _masked_empty_rows_uniform(qr, kr, v, scale, allowed):  # empty rows fall back to dense
+    allowed = allowed | ~allowed.any(axis=1, keepdims=True)
+    return _orig["attention_rows_masked"](qr, kr, v, scale, allowed)
+
+
+def _window_strict(grid, window, qblock=256, kblock=128):  # < instead of <=
+    return _orig["window_block_mask"](grid, tuple(max(0, x - 1) for x in window), qblock, kblock)
+
+
 MUTANTS = {
+    "mask_blocks_swapped": ("block_key_mask", _mask_blocks_swapped),
+    "mask_ignored": ("block_key_mask", _mask_ignored),
+    "masked_empty_rows_dense": ("attention_rows_masked", _masked_empty_rows_uniform),
+    "window_strict": ("window_block_mask", _window_strict),
     "freq_no_two": ("rope_frequencies", _freq_no_two),
     "freq_global_ladder": ("rope_frequencies", _freq_global_ladder),
     "pos_hw_swapped": ("token_positions", _pos_hw_swapped),
