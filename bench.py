@@ -28,6 +28,7 @@ from video_diffusion_transformer_rope_gb300 import configs, synth  # noqa: E402
 KERNEL_SRC = os.path.join(ROOT, "video_diffusion_transformer_rope_gb300", "csrc", "attn_fwd_sm103.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_bf16_sm103_traffic.txt")
 METRIC = "3D-RoPE attention TFLOP/s (4*B*H*N^2*d per call), Wan-14B 720p shape, 1 GB300"
+METRIC_WINDOW = "windowed 3D-RoPE attention TFLOP/s (4*d per kept query-key pair), 1 GB300"
 
 
 def _peaks():
@@ -221,9 +222,27 @@ def run_ours(args, w):
     k_ws = torch.empty(vdx.workspace_bytes(w.B, w.H, grid, w.d, qk) // 2, dtype=torch.float16,
                        device=dev) if args.k_rope == "prepass" else None
 
-    def step():
-        vdx.rope3d_attn(q, k, v, grid, w.sections, w.theta, out=out, lse=lse, stream=stream,
-                        k_rope=k_mode, workspace=k_ws, qk_precision=qk)
+    work = w.flops                       # FLOP per call (dense: 4*B*H*N^2*d)
+    if args.window:
+        # windowed (block-sparse) attention: count only the query-key pairs the mask keeps
+        import numpy as np
+        win = tuple(int(x) for x in args.window.split(","))
+        words = vdx.window_block_mask(grid, win)
+        nk = (w.N + vdx.SPARSE_KBLOCK - 1) // vdx.SPARSE_KBLOCK
+        bits = ((words[:, :, None] >> np.arange(32, dtype=np.uint32)) & 1).reshape(words.shape[0], -1)[:, :nk]
+        qrows = np.minimum(vdx.SPARSE_QBLOCK, w.N - np.arange(words.shape[0]) * vdx.SPARSE_QBLOCK)
+        kcols = np.minimum(vdx.SPARSE_KBLOCK, w.N - np.arange(nk) * vdx.SPARSE_KBLOCK)
+        pairs = float((qrows[:, None] * bits * kcols[None, :]).sum())
+        work = 4.0 * w.B * w.H * pairs * w.d
+        mask_dev = torch.from_numpy(words.astype(np.int32)).to(dev)
+
+        def step():
+            vdx.rope3d_attn_sparse(q, k, v, grid, mask_dev, w.sections, w.theta, out=out, lse=lse,
+                                   stream=stream, workspace=k_ws, qk_precision=qk)
+    else:
+        def step():
+            vdx.rope3d_attn(q, k, v, grid, w.sections, w.theta, out=out, lse=lse, stream=stream,
+                            k_rope=k_mode, workspace=k_ws, qk_precision=qk)
 
     for _ in range(args.warmup):
         step()
@@ -279,14 +298,14 @@ def run_ours(args, w):
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
 
-    tflops_rank = w.flops / (ms * 1e-3) / 1e12
-    value = ws * w.flops / (ms * 1e-3) / 1e12
-    e2e_value = ws * w.flops / (e2e_ms * 1e-3) / 1e12
+    tflops_rank = work / (ms * 1e-3) / 1e12
+    value = ws * work / (ms * 1e-3) / 1e12
+    e2e_value = ws * work / (e2e_ms * 1e-3) / 1e12
     peak, peak_sus, peak_src = _peaks()
     traffic = _traffic_per_launch(w.name)
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.window:
         hq64, hk64, hv64 = hq, hk, hv
         heads, rph = 16, 256
         dt, rows = _cpu_oracle_sample(w, hq64, hk64, hv64, heads, rph)
@@ -297,11 +316,13 @@ def run_ours(args, w):
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+            "metric": METRIC_WINDOW if args.window else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) on device, bf16)",
-            "config": _config(w, args.k_rope),
+            "config": dict(_config(w, args.k_rope), **({"window": args.window,
+                                                         "mask_density": work / w.flops}
+                                                        if args.window else {})),
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": args.steps * (2 if args.k_rope == "prepass" else 1),
@@ -328,6 +349,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=configs.WAN14B_720P.name, choices=sorted(configs.BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--window", default=None,
+                    help="wt,wh,ww: windowed 3D attention through the block-sparse path; value "
+                         "counts only the query-key pairs the window's block mask keeps")
     ap.add_argument("--k-rope", choices=["prepass", "fused"], default="prepass",
                     help="K rotated once by a prepass kernel (default) or per tile inside the "
                          "attention kernel")

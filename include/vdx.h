@@ -34,6 +34,7 @@
 #define VDX_H_
 
 #include <stddef.h>
+#include <stdint.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -96,6 +97,35 @@ vdx_status vdx_rope3d_attn_ex(const void* q, const void* k, const void* v, void*
  * VDX_QK_SPLIT; 0 for invalid sizes. */
 size_t vdx_rope3d_workspace_bytes(int B, int H, int T, int Hgrid, int Wgrid, int d,
                                   int qk_precision);
+
+/* ---- Block-sparse attention (the "bit-wise block-sparse kernel" of ScalingAttention, on the
+ * first thelatestinai.com page of this reference; masks here are caller-defined).  Keys are
+ * cut into tiles of VDX_SPARSE_KBLOCK tokens and queries into blocks of VDX_SPARSE_QBLOCK
+ * tokens; query n attends only to the key tiles its block's mask selects (a query whose mask
+ * row selects nothing gets out = 0 and lse = -inf).  Skipped tiles cost no work.
+ *   block_mask: device uint32 words, row-major [M][n_qblocks][W] with
+ *     W = vdx_rope3d_block_mask_words(T, Hgrid, Wgrid), n_qblocks = ceil(N / 256),
+ *     M = B*H (mask_per_head = 1, one mask per (b, h)) or 1 (mask_per_head = 0, shared);
+ *     bit (kb % 32) of word kb / 32 selects key tile kb; bits at or beyond ceil(N/128) ignored.
+ *   Other arguments, rules and options as vdx_rope3d_attn_ex (K prepass only). */
+#define VDX_SPARSE_QBLOCK 256
+#define VDX_SPARSE_KBLOCK 128
+vdx_status vdx_rope3d_attn_sparse(const void* q, const void* k, const void* v, void* out,
+                                  float* lse, int B, int H, int T, int Hgrid, int Wgrid, int d,
+                                  int sec_t, int sec_h, int sec_w, double theta, float scale,
+                                  const uint32_t* block_mask, int mask_per_head,
+                                  const vdx_attn_options* opt, void* stream);
+
+/* Words per query block of a block mask for this grid (ceil(ceil(N/128)/32)); 0 if invalid. */
+int vdx_rope3d_block_mask_words(int T, int Hgrid, int Wgrid);
+
+/* Host helper: fill `mask` (host memory, [n_qblocks][W] words) with the block mask of 3D
+ * windowed attention (the windowed-attention primitive of the vidax page, §2 "3D RoPE, 3D
+ * VAEs, and flash attention"), at block granularity: query block Qb selects key tile Kb when
+ * some token of Qb and some token of Kb are within (wt, wh, ww) of each other on every grid
+ * axis (|dt| <= wt, |dh| <= wh, |dw| <= ww).  Pass it with mask_per_head = 0. */
+vdx_status vdx_window_block_mask(uint32_t* mask, int T, int Hgrid, int Wgrid, int wt, int wh,
+                                 int ww);
 
 /* fp32 path (CUDA cores, fp32 arithmetic throughout).  Same operation and rules; q, k, v,
  * out are float [B, N, H, d]; d must be 64 or 128. */

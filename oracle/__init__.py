@@ -3,4 +3,4 @@ from .fp64 import (default_sections, token_positions, rope_frequencies,  # noqa:
                                rope3d_angles, apply_rotary, rope3d, attention_rows,
                                rope3d_attention, rope3d_attention_rows,
                    block_key_mask, attention_rows_masked, rope3d_attention_blocksparse,
-                   window_block_mask)
+                   window_block_mask, rope3d_attention_blocksparse_rows)

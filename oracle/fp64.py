@@ -240,3 +240,37 @@ def window_block_mask(grid, window, qblock=256, kblock=128):
                     (np.abs(w[qs][:, None] - w[ks][None, :]) <= ww))
             mask[qb, kb] = bool(near.any())
     return mask
+
+
+def rope3d_attention_blocksparse_rows(q, k, v, grid, rows, mask, qblock=256, kblock=128,
+                                      sections=None, theta=10000.0, scale=None):
+    """Block-sparse oracle on selected query rows (b, h, n); returns (o [R, d], lse [R])."""
+    B, N, H, d = q.shape
+    sections = tuple(sections) if sections else default_sections(d)
+    scale = d ** -0.5 if scale is None else scale
+    mask = np.asarray(mask, dtype=bool)
+    T, Hg, Wg = grid
+    pt, ph, pw = token_positions(T, Hg, Wg)
+    by_head = {}
+    for i, (b, h, n) in enumerate(rows):
+        by_head.setdefault((b, h), []).append((i, n))
+    o = np.empty((len(rows), d))
+    lse = np.empty(len(rows))
+    kb_of = np.arange(N) // kblock
+    for (b, h), items in by_head.items():
+        kr = apply_rotary(_to64(k[b, :, h, :]), rope3d_angles(pt, ph, pw, sections, theta))
+        vh = _to64(v[b, :, h, :])
+        mk = mask if mask.ndim == 2 else mask[b, h]
+        idx = np.array([n for _, n in items])
+        if hasattr(q, "detach"):
+            import torch
+            qh = _to64(q[b, :, h, :][torch.from_numpy(idx).to(q.device)])
+        else:
+            qh = _to64(q[b, idx, h, :])
+        qr = apply_rotary(qh, rope3d_angles(pt[idx], ph[idx], pw[idx], sections, theta))
+        allowed = mk[(idx // qblock)[:, None], kb_of[None, :]]
+        oo, ll = attention_rows_masked(qr, kr, vh, scale, allowed)
+        for j, (i, _) in enumerate(items):
+            o[i] = oo[j]
+            lse[i] = ll[j]
+    return o, lse

@@ -339,4 +339,19 @@ def pin_window_block_mask_brute_force(O):
     assert O.window_block_mask(grid, (T, Hg, Wg)).all()
 
 
+def pin_blocksparse_rows_match_full(O):
+    """The sampled-row block-sparse entry gives the full block-sparse oracle's rows."""
+    B, H, d, grid = 2, 2, 64, (2, 5, 60)
+    N = 600
+    q, k, v, _, _ = _rotated(O, B, N, H, d, grid, 17)
+    mask = _rng(18).random((B, H, 3, 5)) < 0.5
+    mask[0, 1, 2] = False                      # an empty query block
+    out, lse = O.rope3d_attention_blocksparse(q, k, v, grid, mask)
+    rows = [(0, 0, 0), (1, 1, 599), (0, 1, 550), (1, 0, 300), (0, 1, 511)]
+    o, l = O.rope3d_attention_blocksparse_rows(q, k, v, grid, rows, mask)
+    for i, (b, h, n) in enumerate(rows):
+        assert np.allclose(o[i], out[b, n, h], atol=1e-14, rtol=0)
+        assert (np.isneginf(l[i]) and np.isneginf(lse[b, h, n])) or abs(l[i] - lse[b, h, n]) < 1e-14
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

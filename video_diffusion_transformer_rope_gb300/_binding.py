@@ -30,6 +30,10 @@ SIGNATURES = {
                                 ctypes.POINTER(AttnOptions), _p]),
     "vdx_rope3d_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i, _i]),
     "vdx_rope3d_attn_f32": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f, _p]),
+    "vdx_rope3d_attn_sparse": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f,
+                                    _p, _i, ctypes.POINTER(AttnOptions), _p]),
+    "vdx_rope3d_block_mask_words": (_i, [_i, _i, _i]),
+    "vdx_window_block_mask": (_i, [_p, _i, _i, _i, _i, _i, _i]),
     "vdx_rope3d_attn_noalloc": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f, _p]),
     "vdx_sync_check": (_i, [_p]),
     "vdx_last_error": (ctypes.c_char_p, []),
@@ -119,6 +123,84 @@ def rope3d_attn(q, k, v, grid, sections=(0, 0, 0), theta=10000.0, scale=0.0, out
         _check(lib().vdx_rope3d_attn_f32(*args))
     else:
         raise VdxError(VDX_ERR_UNSUPPORTED, f"dtype {q.dtype} (use bfloat16 or float32)")
+    return out, lse
+
+
+SPARSE_QBLOCK, SPARSE_KBLOCK = 256, 128
+
+
+def block_mask_words(grid):
+    """uint32 words per query block of a block mask for this grid."""
+    T, Hg, Wg = (int(x) for x in grid)
+    return lib().vdx_rope3d_block_mask_words(T, Hg, Wg)
+
+
+def pack_block_mask(mask_bool):
+    """Pack a boolean block mask [..., n_qblocks, n_kblocks] into uint32 words
+    [..., n_qblocks, ceil(n_kblocks / 32)] (bit kb % 32 of word kb // 32)."""
+    import numpy as np
+    m = np.asarray(mask_bool, dtype=bool)
+    nk = m.shape[-1]
+    words = (nk + 31) // 32
+    pad = np.zeros(m.shape[:-1] + (words * 32,), dtype=bool)
+    pad[..., :nk] = m
+    bits = pad.reshape(m.shape[:-1] + (words, 32)).astype(np.uint64)
+    return (bits << np.arange(32, dtype=np.uint64)).sum(axis=-1).astype(np.uint32)
+
+
+def window_block_mask(grid, window):
+    """Block mask of 3D windowed attention (host numpy uint32 [n_qblocks, words]), built by
+    the library's vdx_window_block_mask."""
+    import numpy as np
+    T, Hg, Wg = (int(x) for x in grid)
+    N = T * Hg * Wg
+    nqb = (N + SPARSE_QBLOCK - 1) // SPARSE_QBLOCK
+    out = np.zeros((nqb, block_mask_words(grid)), dtype=np.uint32)
+    wt, wh, ww = (int(x) for x in window)
+    _check(lib().vdx_window_block_mask(out.ctypes.data_as(ctypes.c_void_p), T, Hg, Wg, wt, wh, ww))
+    return out
+
+
+def rope3d_attn_sparse(q, k, v, grid, block_mask, sections=(0, 0, 0), theta=10000.0, scale=0.0,
+                       out=None, lse=None, return_lse=True, stream=None, workspace=None,
+                       qk_precision=QK_FP16):
+    """Block-sparse 3D-RoPE attention (bf16, d = 128).  block_mask: CUDA uint32/int32 tensor of
+    packed words, shape [B, H, n_qblocks, W] (one mask per head) or [n_qblocks, W] (shared);
+    see pack_block_mask / window_block_mask."""
+    import torch
+    T, Hg, Wg = (int(x) for x in grid)
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape or q.dtype != torch.bfloat16:
+        raise VdxError(VDX_ERR_ARG, "q, k, v must be bf16 [B, N, H, d] tensors of one shape")
+    B, N, H, d = q.shape
+    if N != T * Hg * Wg:
+        raise VdxError(VDX_ERR_ARG, f"N={N} does not match grid {T}x{Hg}x{Wg}")
+    nqb = (N + SPARSE_QBLOCK - 1) // SPARSE_QBLOCK
+    W = block_mask_words(grid)
+    if block_mask.dtype not in (torch.int32, torch.uint32) or not block_mask.is_cuda or not block_mask.is_contiguous():
+        raise VdxError(VDX_ERR_ARG, "block_mask must be a contiguous CUDA int32/uint32 tensor")
+    if tuple(block_mask.shape) == (B, H, nqb, W):
+        per_head = 1
+    elif tuple(block_mask.shape) == (nqb, W):
+        per_head = 0
+    else:
+        raise VdxError(VDX_ERR_ARG, f"block_mask shape {tuple(block_mask.shape)} is neither "
+                                    f"{(B, H, nqb, W)} nor {(nqb, W)}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise VdxError(VDX_ERR_ARG, f"{name} must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    st, sh, sw = (int(x) for x in sections)
+    opt = AttnOptions(K_ROPE_PREPASS, int(qk_precision),
+                      ctypes.c_void_p(workspace.data_ptr() if workspace is not None else 0),
+                      workspace.numel() * workspace.element_size() if workspace is not None else 0)
+    _check(lib().vdx_rope3d_attn_sparse(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+        ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr() if lse is not None else 0),
+        B, H, T, Hg, Wg, d, st, sh, sw, float(theta), float(scale),
+        ctypes.c_void_p(block_mask.data_ptr()), per_head, ctypes.byref(opt), _stream_handle(stream)))
     return out, lse
 
 

@@ -110,6 +110,10 @@ struct Ctl {
 
 struct Params {
   int B, H, N, Hg, Wg, HgWg;
+  // Optional block mask: bit kb of word kb/32 of row (b, h, query block) selects key tile kb.
+  const uint32_t* kv_mask;     // nullptr: every key tile
+  int mask_words;              // words per query block
+  long long mask_bh_stride;    // words between consecutive (b, h) masks (0: one shared mask)
   int half_t, half_h, half_w;
   int off_h, off_w;            // table offsets of the h and w blocks (entries)
   int table_entries;
@@ -257,6 +261,38 @@ __device__ __forceinline__ float rope_tile(const Params& p, const RopeLane& L, i
   return amax;
 }
 
+// The key tiles a CTA visits, in increasing order: all nkv of them, or the tiles whose bit is
+// set in its mask row (bits at or beyond nkv are ignored).  Every role walks the same sequence.
+struct TileCursor {
+  const uint32_t* row;   // nullptr: dense
+  int nkv, word, words;
+  uint32_t bits;
+  int t;
+  __device__ __forceinline__ uint32_t word_bits(int w) const {
+    uint32_t x = __ldg(row + w);
+    const int hi = nkv - 32 * w;            // valid bits in this word
+    return hi >= 32 ? x : (x & ((1u << hi) - 1u));
+  }
+  __device__ __forceinline__ void init(const uint32_t* r, int n_kv, int n_words) {
+    row = r; nkv = n_kv; words = n_words; word = 0; t = 0;
+    bits = row ? word_bits(0) : 0u;
+  }
+  __device__ __forceinline__ int count() const {
+    if (!row) return nkv;
+    int c = 0;
+    for (int w = 0; w < words; ++w) c += __popc(word_bits(w));
+    return c;
+  }
+  // Next tile index; only called count() times.
+  __device__ __forceinline__ int next() {
+    if (!row) return t++;
+    while (bits == 0) bits = word_bits(++word);
+    const int b = __ffs(bits) - 1;
+    bits &= bits - 1u;
+    return word * 32 + b;
+  }
+};
+
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -282,7 +318,14 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const int b = bh / p.H;
   const int h = bh - b * p.H;
   const int q0 = qblk * kRowsPerCta;
-  const int nkv = (p.N + kBN - 1) / kBN;
+  const int nkv_all = (p.N + kBN - 1) / kBN;
+  const uint32_t* mask_row =
+      p.kv_mask ? p.kv_mask + (static_cast<long long>(bh) * p.mask_bh_stride +
+                               static_cast<long long>(qblk) * p.mask_words)
+                : nullptr;
+  TileCursor cur;
+  cur.init(mask_row, nkv_all, p.mask_words);
+  const int nkv = cur.count();              // key tiles this CTA visits (steps j = 0..nkv-1)
 
   const uint32_t sQ = smem_addr(smem + Lo::kOffQ);
   const uint32_t sK = smem_addr(smem + Lo::kOffK);
@@ -338,6 +381,7 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < nkv; ++j) {
+        const int kt = cur.next();          // key tile of step j
         const int ks = j % kKStages, ku = j / kKStages;
         if (ku > 0 && !mbar_wait(smem_addr(&ctl->k_empty[ks]), (ku - 1) & 1, abort_flag, kSiteKEmpty))
           break;
@@ -345,11 +389,11 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           const uint32_t bar = smem_addr(&ctl->k_full[ks]);
           mbar_arrive_expect_tx(bar, Lo::kKStageBytes);
           const uint32_t dst = sK + ks * Lo::kKStageBytes;
-          tma_load_4d(dst, &tm_k, bar, 0, h, j * kBN, b);
-          tma_load_4d(dst + kHalfBytes, &tm_k, bar, 64, h, j * kBN, b);
+          tma_load_4d(dst, &tm_k, bar, 0, h, kt * kBN, b);
+          tma_load_4d(dst + kHalfBytes, &tm_k, bar, 64, h, kt * kBN, b);
           if (kSplit) {
-            tma_load_4d(dst + kTileBytes, &tm_klo, bar, 0, h, j * kBN, b);
-            tma_load_4d(dst + kTileBytes + kHalfBytes, &tm_klo, bar, 64, h, j * kBN, b);
+            tma_load_4d(dst + kTileBytes, &tm_klo, bar, 0, h, kt * kBN, b);
+            tma_load_4d(dst + kTileBytes + kHalfBytes, &tm_klo, bar, 64, h, kt * kBN, b);
           }
           k_issued = j + 1;
         }
@@ -360,8 +404,8 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           const uint32_t bar = smem_addr(&ctl->v_full[vs]);
           mbar_arrive_expect_tx(bar, kTileBytes);
           const uint32_t dst = sV + vs * kTileBytes;
-          tma_load_4d(dst, &tm_v, bar, 0, h, j * kBN, b);
-          tma_load_4d(dst + kHalfBytes, &tm_v, bar, 64, h, j * kBN, b);
+          tma_load_4d(dst, &tm_v, bar, 0, h, kt * kBN, b);
+          tma_load_4d(dst + kHalfBytes, &tm_v, bar, 64, h, kt * kBN, b);
           v_issued = j + 1;
         }
       }
@@ -424,7 +468,7 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tc_fence_after_sync();
         issue_pv(tO0, tS0, sV + vs * kTileBytes, kIdPV, j > 0);
       }
-      if (ok) {
+      if (ok && nkv > 0) {
         const int jl = nkv - 1;
         if (__all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->p_ready[1]), jl & 1, abort_flag, kSitePReady))) {
           tc_fence_after_sync();
@@ -452,10 +496,11 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     if (kFusedK) {
       for (int j = 0; ok && j < nkv; ++j) {
+        const int kt = cur.next();
         const int ks = j % kKStages;
         if (!(ok = mbar_wait(smem_addr(&ctl->k_full[ks]), (j / kKStages) & 1, abort_flag, kSiteKFull)))
           break;
-        amax = fmaxf(amax, rope_tile<false>(p, L, t, smem + Lo::kOffK + ks * Lo::kKStageBytes, j * kBN, tab));
+        amax = fmaxf(amax, rope_tile<false>(p, L, t, smem + Lo::kOffK + ks * Lo::kKStageBytes, kt * kBN, tab));
         fence_proxy_async_smem();
         mbar_arrive(smem_addr(&ctl->k_ready[ks]));
       }
@@ -475,11 +520,12 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     float l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
+      const int kt = cur.next();
       if (!(ok = mbar_wait(smem_addr(&ctl->s_full[qi]), j & 1, abort_flag, kSiteSFull))) break;
       tc_fence_after_sync();
       uint32_t s[128];
       tmem_ld128(tS, s);
-      const int valid = p.N - j * kBN;
+      const int valid = p.N - kt * kBN;
       if (valid < kBN) {             // ragged last tile: keys beyond N weigh nothing
 #pragma unroll
         for (int e = 0; e < 128; ++e)
@@ -553,12 +599,19 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       tc_fence_after_sync();
       const int n = q0 + qi * kBM + row;
       const bool live = n < p.N;
-      const float inv_l = 1.f / l_run;
+      // A query block whose mask selects no key tile has no keys: out = 0, lse = -inf.
+      const bool empty = nkv == 0;
+      const float inv_l = empty ? 0.f : 1.f / l_run;
       __nv_bfloat16* orow = p.out + ((static_cast<size_t>(b) * p.N + (live ? n : 0)) * p.H + h) * kD;
       uint32_t r[32];
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
-        tmem_ld32(tO + ch * 32, r);
+        if (empty) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = 0u;
+        } else {
+          tmem_ld32(tO + ch * 32, r);
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int e2 = 0; e2 < 16; ++e2)
@@ -571,7 +624,8 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
       }
       if (live && p.lse != nullptr)
-        p.lse[(static_cast<size_t>(b) * p.H + h) * p.N + n] = (m_run + __log2f(l_run)) * 0.69314718055994530942f;
+        p.lse[(static_cast<size_t>(b) * p.H + h) * p.N + n] =
+            empty ? -INFINITY : (m_run + __log2f(l_run)) * 0.69314718055994530942f;
     }
   }
 
@@ -621,6 +675,9 @@ void fill_params(const Problem& pr, Params* p) {
   p->table = pr.table;
   p->out = static_cast<__nv_bfloat16*>(pr.out);
   p->lse = pr.lse;
+  p->kv_mask = pr.kv_mask;
+  p->mask_words = pr.mask_words;
+  p->mask_bh_stride = pr.mask_bh_stride;
 }
 
 CUresult encode_bhnd(EncodeTiledFn encode, CUtensorMap* map, const void* base,

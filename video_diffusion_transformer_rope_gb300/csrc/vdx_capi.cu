@@ -12,6 +12,8 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdint>
+#include <cstdlib>
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <string>
@@ -193,10 +195,10 @@ void set_last_error(const char* message) { t_last_error = message; }
 
 extern "C" {
 
-vdx_status vdx_rope3d_attn_ex(const void* q, const void* k, const void* v, void* out, float* lse,
-                              int B, int H, int T, int Hgrid, int Wgrid, int d, int sec_t,
-                              int sec_h, int sec_w, double theta, float scale,
-                              const vdx_attn_options* opt, void* stream) {
+static vdx_status attn_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
+                            int B, int H, int T, int Hgrid, int Wgrid, int d, int sec_t, int sec_h,
+                            int sec_w, double theta, float scale, const vdx_attn_options* opt,
+                            const uint32_t* block_mask, int mask_per_head, void* stream) {
   t_last_error.clear();
   if (d != 128) return fail(VDX_ERR_UNSUPPORTED, "bf16 path supports head_dim 128 only (got %d)", d);
   const int mode = opt ? opt->k_rope : VDX_K_ROPE_DEFAULT;
@@ -213,6 +215,15 @@ vdx_status vdx_rope3d_attn_ex(const void* q, const void* k, const void* v, void*
   vdx_status s = prepare(q, k, v, out, lse, B, H, T, Hgrid, Wgrid, d, sec_t, sec_h, sec_w, theta,
                          scale, 2, &p);
   if (s != VDX_OK) return s;
+  if (block_mask) {
+    if (reinterpret_cast<uintptr_t>(block_mask) & 3)
+      return fail(VDX_ERR_ALIGN, "block_mask is not 4-byte aligned");
+    const int nkv = (p.N + VDX_SPARSE_KBLOCK - 1) / VDX_SPARSE_KBLOCK;
+    const int nqb = (p.N + VDX_SPARSE_QBLOCK - 1) / VDX_SPARSE_QBLOCK;
+    p.kv_mask = block_mask;
+    p.mask_words = (nkv + 31) / 32;
+    p.mask_bh_stride = mask_per_head ? static_cast<long long>(nqb) * p.mask_words : 0;
+  }
   void* ws = nullptr;
   if (!fused) {
     const size_t need = vdx::k_prepass_workspace_bytes(p, split);
@@ -241,11 +252,96 @@ vdx_status vdx_rope3d_attn_ex(const void* q, const void* k, const void* v, void*
   return VDX_OK;
 }
 
+vdx_status vdx_rope3d_attn_ex(const void* q, const void* k, const void* v, void* out, float* lse,
+                              int B, int H, int T, int Hgrid, int Wgrid, int d, int sec_t,
+                              int sec_h, int sec_w, double theta, float scale,
+                              const vdx_attn_options* opt, void* stream) {
+  return attn_bf16(q, k, v, out, lse, B, H, T, Hgrid, Wgrid, d, sec_t, sec_h, sec_w, theta, scale,
+                   opt, nullptr, 0, stream);
+}
+
 vdx_status vdx_rope3d_attn(const void* q, const void* k, const void* v, void* out, float* lse,
                            int B, int H, int T, int Hgrid, int Wgrid, int d, int sec_t, int sec_h,
                            int sec_w, double theta, float scale, void* stream) {
   return vdx_rope3d_attn_ex(q, k, v, out, lse, B, H, T, Hgrid, Wgrid, d, sec_t, sec_h, sec_w,
                             theta, scale, nullptr, stream);
+}
+
+vdx_status vdx_rope3d_attn_sparse(const void* q, const void* k, const void* v, void* out,
+                                  float* lse, int B, int H, int T, int Hgrid, int Wgrid, int d,
+                                  int sec_t, int sec_h, int sec_w, double theta, float scale,
+                                  const uint32_t* block_mask, int mask_per_head,
+                                  const vdx_attn_options* opt, void* stream) {
+  if (!block_mask) {
+    t_last_error.clear();
+    return fail(VDX_ERR_ARG, "block_mask must be non-NULL");
+  }
+  if (opt && opt->k_rope == VDX_K_ROPE_FUSED) {
+    t_last_error.clear();
+    // fused K rotation is kept for the dense call only
+    return fail(VDX_ERR_UNSUPPORTED, "block-sparse calls use the K prepass");
+  }
+  return attn_bf16(q, k, v, out, lse, B, H, T, Hgrid, Wgrid, d, sec_t, sec_h, sec_w, theta, scale,
+                   opt, block_mask, mask_per_head, stream);
+}
+
+int vdx_rope3d_block_mask_words(int T, int Hgrid, int Wgrid) {
+  if (T < 1 || Hgrid < 1 || Wgrid < 1) return 0;
+  const long long N = static_cast<long long>(T) * Hgrid * Wgrid;
+  const long long nkv = (N + VDX_SPARSE_KBLOCK - 1) / VDX_SPARSE_KBLOCK;
+  return static_cast<int>((nkv + 31) / 32);
+}
+
+vdx_status vdx_window_block_mask(uint32_t* mask, int T, int Hgrid, int Wgrid, int wt, int wh,
+                                 int ww) {
+  t_last_error.clear();
+  if (!mask) return fail(VDX_ERR_ARG, "mask must be non-NULL");
+  if (T < 1 || Hgrid < 1 || Wgrid < 1) return fail(VDX_ERR_ARG, "grid extents must be >= 1");
+  if (wt < 0 || wh < 0 || ww < 0) return fail(VDX_ERR_ARG, "window half-widths must be >= 0");
+  const long long N = static_cast<long long>(T) * Hgrid * Wgrid;
+  if (N > 0x3fffffffLL) return fail(VDX_ERR_ARG, "grid too large");
+  const int HW = Hgrid * Wgrid;
+  // A block of consecutive tokens is a few runs along w: (t, h, w0..w1).
+  struct Run { int t, h, w0, w1; };
+  auto runs_of = [&](long long start, long long end, std::vector<Run>& out) {
+    out.clear();
+    for (long long n = start; n < end;) {
+      const int t = static_cast<int>(n / HW), h = static_cast<int>((n / Wgrid) % Hgrid);
+      const int w0 = static_cast<int>(n % Wgrid);
+      const int w1 = static_cast<int>(std::min<long long>(Wgrid - 1, w0 + (end - 1 - n)));
+      out.push_back({t, h, w0, w1});
+      n += w1 - w0 + 1;
+    }
+  };
+  const int nkv = static_cast<int>((N + VDX_SPARSE_KBLOCK - 1) / VDX_SPARSE_KBLOCK);
+  const int nqb = static_cast<int>((N + VDX_SPARSE_QBLOCK - 1) / VDX_SPARSE_QBLOCK);
+  const int words = (nkv + 31) / 32;
+  std::vector<std::vector<Run>> kruns(nkv);
+  for (int kb = 0; kb < nkv; ++kb)
+    runs_of(static_cast<long long>(kb) * VDX_SPARSE_KBLOCK,
+            std::min<long long>(N, static_cast<long long>(kb + 1) * VDX_SPARSE_KBLOCK), kruns[kb]);
+  std::vector<Run> qruns;
+  for (int qb = 0; qb < nqb; ++qb) {
+    runs_of(static_cast<long long>(qb) * VDX_SPARSE_QBLOCK,
+            std::min<long long>(N, static_cast<long long>(qb + 1) * VDX_SPARSE_QBLOCK), qruns);
+    uint32_t* row = mask + static_cast<size_t>(qb) * words;
+    for (int w = 0; w < words; ++w) row[w] = 0u;
+    for (int kb = 0; kb < nkv; ++kb) {
+      bool near = false;
+      for (const Run& a : qruns) {
+        for (const Run& c : kruns[kb]) {
+          if (std::abs(a.t - c.t) <= wt && std::abs(a.h - c.h) <= wh && a.w0 <= c.w1 + ww &&
+              c.w0 <= a.w1 + ww) {
+            near = true;
+            break;
+          }
+        }
+        if (near) break;
+      }
+      if (near) row[kb / 32] |= 1u << (kb % 32);
+    }
+  }
+  return VDX_OK;
 }
 
 size_t vdx_rope3d_workspace_bytes(int B, int H, int T, int Hgrid, int Wgrid, int d,

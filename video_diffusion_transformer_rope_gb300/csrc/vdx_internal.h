@@ -22,6 +22,11 @@ struct Problem {
   float scale;
   const float2* table;
   int table_entries;
+  // Optional block mask (device): row (b, h, query block of 256) at word offset
+  // (b*H + h) * mask_bh_stride + qblock * mask_words; bit kb of word kb/32 selects key tile kb.
+  const uint32_t* kv_mask = nullptr;
+  int mask_words = 0;
+  long long mask_bh_stride = 0;
 };
 
 // bf16, d = 128, tcgen05 kernel (attn_fwd_sm103.cu).  `encode` is cuTensorMapEncodeTiled.
