@@ -29,6 +29,7 @@ KERNEL_SRC = os.path.join(ROOT, "video_diffusion_transformer_rope_gb300", "csrc"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_bf16_sm103_traffic.txt")
 METRIC = "3D-RoPE attention TFLOP/s (4*B*H*N^2*d per call), Wan-14B 720p shape, 1 GB300"
 METRIC_WINDOW = "windowed 3D-RoPE attention TFLOP/s (4*d per kept query-key pair), 1 GB300"
+METRIC_SUBSET = "active-query 3D-RoPE attention TFLOP/s (4*d per active query-key pair), 1 GB300"
 
 
 def _peaks():
@@ -239,6 +240,17 @@ def run_ours(args, w):
         def step():
             vdx.rope3d_attn_sparse(q, k, v, grid, mask_dev, w.sections, w.theta, out=out, lse=lse,
                                    stream=stream, workspace=k_ws, qk_precision=qk)
+    elif args.subset:
+        # active-query subset: a seeded fraction of the tokens attends to every key
+        frac = float(args.subset)
+        nq = max(1, int(round(frac * w.N)))
+        gsub = torch.Generator(device="cpu").manual_seed(w.seed + 3000)
+        idx = torch.randperm(w.N, generator=gsub)[:nq].sort().values.to(torch.int32).to(dev)
+        work = 4.0 * w.B * w.H * float(nq) * w.N * w.d
+
+        def step():
+            vdx.rope3d_attn_subset(q, k, v, grid, idx, out, lse, w.sections, w.theta,
+                                   stream=stream, workspace=k_ws, qk_precision=qk)
     else:
         def step():
             vdx.rope3d_attn(q, k, v, grid, w.sections, w.theta, out=out, lse=lse, stream=stream,
@@ -305,7 +317,7 @@ def run_ours(args, w):
     traffic = _traffic_per_launch(w.name)
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.window:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.window and not args.subset:
         hq64, hk64, hv64 = hq, hk, hv
         heads, rph = 16, 256
         dt, rows = _cpu_oracle_sample(w, hq64, hk64, hv64, heads, rph)
@@ -316,13 +328,15 @@ def run_ours(args, w):
 
     if rank == 0:
         line = {
-            "metric": METRIC_WINDOW if args.window else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+            "metric": METRIC_WINDOW if args.window else (METRIC_SUBSET if args.subset else METRIC),
+            "value": value, "unit": "TFLOP/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) on device, bf16)",
             "config": dict(_config(w, args.k_rope), **({"window": args.window,
                                                          "mask_density": work / w.flops}
-                                                        if args.window else {})),
+                                                        if args.window else {}),
+                           **({"active_query_fraction": float(args.subset)} if args.subset else {})),
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": args.steps * (2 if args.k_rope == "prepass" else 1),
@@ -352,6 +366,9 @@ def main():
     ap.add_argument("--window", default=None,
                     help="wt,wh,ww: windowed 3D attention through the block-sparse path; value "
                          "counts only the query-key pairs the window's block mask keeps")
+    ap.add_argument("--subset", default=None,
+                    help="fraction: active-query subset (that share of tokens, seeded) attends to "
+                         "every key; value counts 4*d per active query-key pair")
     ap.add_argument("--k-rope", choices=["prepass", "fused"], default="prepass",
                     help="K rotated once by a prepass kernel (default) or per tile inside the "
                          "attention kernel")

@@ -116,6 +116,20 @@ vdx_status vdx_rope3d_attn_sparse(const void* q, const void* k, const void* v, v
                                   const uint32_t* block_mask, int mask_per_head,
                                   const vdx_attn_options* opt, void* stream);
 
+/* ---- Active-query subset (after the step-skipping scheme on the first thelatestinai.com page
+ * of this reference, where only active query tokens are recomputed against the full K/V).
+ * Query rows are the tokens q_index[i], i < Nq (device int32; one list shared by every batch
+ * entry when index_per_batch = 0, else [B][Nq]); each is rotated at its own grid position,
+ * attends to all N keys, and its result is written to out[b, q_index[i], h, :] and
+ * lse[b, h, q_index[i]].  Rows of out / lse not listed are left untouched.  An index outside
+ * [0, N) is skipped and reported by vdx_sync_check (VDX_ERR_ARG).  Duplicate indices write
+ * the same values twice.  Other arguments, rules and options as vdx_rope3d_attn_ex. */
+vdx_status vdx_rope3d_attn_subset(const void* q, const void* k, const void* v, void* out,
+                                  float* lse, int B, int H, int T, int Hgrid, int Wgrid, int d,
+                                  int sec_t, int sec_h, int sec_w, double theta, float scale,
+                                  const int32_t* q_index, int Nq, int index_per_batch,
+                                  const vdx_attn_options* opt, void* stream);
+
 /* Words per query block of a block mask for this grid (ceil(ceil(N/128)/32)); 0 if invalid. */
 int vdx_rope3d_block_mask_words(int T, int Hgrid, int Wgrid);
 
@@ -158,7 +172,8 @@ vdx_status vdx_rope3d_attn_noalloc(const void* q, const void* k, const void* v, 
 /* Synchronise `stream`, then read and clear the device error word.  Returns VDX_OK,
  * VDX_ERR_TIMEOUT (a kernel gave up on a pipeline wait; the output of that call is
  * undefined), VDX_ERR_RANGE (a rotated q/k value was clamped to the fp16 range; the output
- * is inexact) or VDX_ERR_CUDA (an asynchronous CUDA error is pending). */
+ * is inexact), VDX_ERR_ARG (a q_index entry was out of range; its row was skipped) or
+ * VDX_ERR_CUDA (an asynchronous CUDA error is pending). */
 vdx_status vdx_sync_check(void* stream);
 
 /* Message for the last non-OK status returned on this host thread ("" if none). */

@@ -32,6 +32,8 @@ SIGNATURES = {
     "vdx_rope3d_attn_f32": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f, _p]),
     "vdx_rope3d_attn_sparse": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f,
                                     _p, _i, ctypes.POINTER(AttnOptions), _p]),
+    "vdx_rope3d_attn_subset": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f,
+                                    _p, _i, _i, ctypes.POINTER(AttnOptions), _p]),
     "vdx_rope3d_block_mask_words": (_i, [_i, _i, _i]),
     "vdx_window_block_mask": (_i, [_p, _i, _i, _i, _i, _i, _i]),
     "vdx_rope3d_attn_noalloc": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f, _p]),
@@ -201,6 +203,41 @@ def rope3d_attn_sparse(q, k, v, grid, block_mask, sections=(0, 0, 0), theta=1000
         ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr() if lse is not None else 0),
         B, H, T, Hg, Wg, d, st, sh, sw, float(theta), float(scale),
         ctypes.c_void_p(block_mask.data_ptr()), per_head, ctypes.byref(opt), _stream_handle(stream)))
+    return out, lse
+
+
+def rope3d_attn_subset(q, k, v, grid, q_index, out, lse=None, sections=(0, 0, 0), theta=10000.0,
+                       scale=0.0, stream=None, workspace=None, qk_precision=QK_FP16):
+    """Active-query subset: the tokens in q_index (CUDA int32, [Nq] shared or [B, Nq]) attend to
+    every key; their rows of `out` ([B, N, H, d], written in place) and `lse` ([B, H, N] or None)
+    are updated, all other rows are left as they are."""
+    import torch
+    T, Hg, Wg = (int(x) for x in grid)
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape or q.dtype != torch.bfloat16:
+        raise VdxError(VDX_ERR_ARG, "q, k, v must be bf16 [B, N, H, d] tensors of one shape")
+    B, N, H, d = q.shape
+    if N != T * Hg * Wg:
+        raise VdxError(VDX_ERR_ARG, f"N={N} does not match grid {T}x{Hg}x{Wg}")
+    if q_index.dtype != torch.int32 or not q_index.is_cuda or not q_index.is_contiguous():
+        raise VdxError(VDX_ERR_ARG, "q_index must be a contiguous CUDA int32 tensor")
+    if q_index.dim() == 1:
+        per_batch, Nq = 0, q_index.shape[0]
+    elif q_index.dim() == 2 and q_index.shape[0] == B:
+        per_batch, Nq = 1, q_index.shape[1]
+    else:
+        raise VdxError(VDX_ERR_ARG, f"q_index shape {tuple(q_index.shape)} is neither [Nq] nor [B, Nq]")
+    if out is None or out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise VdxError(VDX_ERR_ARG, "out must be a contiguous bf16 tensor shaped like q")
+    st, sh, sw = (int(x) for x in sections)
+    opt = AttnOptions(K_ROPE_PREPASS, int(qk_precision),
+                      ctypes.c_void_p(workspace.data_ptr() if workspace is not None else 0),
+                      workspace.numel() * workspace.element_size() if workspace is not None else 0)
+    _check(lib().vdx_rope3d_attn_subset(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+        ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr() if lse is not None else 0),
+        B, H, T, Hg, Wg, d, st, sh, sw, float(theta), float(scale),
+        ctypes.c_void_p(q_index.data_ptr()), int(Nq), per_batch, ctypes.byref(opt),
+        _stream_handle(stream)))
     return out, lse
 
 

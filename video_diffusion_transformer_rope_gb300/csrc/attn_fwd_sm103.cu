@@ -81,9 +81,9 @@ struct Layout {
   static constexpr int kOffTab = kOffV + kVStages * kTileBytes;
   // Registers per thread after the role split (sum over the 4 warpgroups = 512 x 128 at
   // launch); the split mode's MMA warp issues three QK chains and needs more.
-  static constexpr uint32_t kRegsSoftmax = kSplit ? 176 : 192;
-  static constexpr uint32_t kRegsRope = 56;
-  static constexpr uint32_t kRegsCtl = kSplit ? 104 : 72;
+  static constexpr uint32_t kRegsSoftmax = kSplit ? 160 : 184;
+  static constexpr uint32_t kRegsRope = kSplit ? 64 : 72;
+  static constexpr uint32_t kRegsCtl = kSplit ? 128 : 72;
   static_assert(2 * kRegsSoftmax + kRegsRope + kRegsCtl <= 4 * 128, "register split over budget");
 };
 
@@ -111,6 +111,12 @@ struct Ctl {
 struct Params {
   int B, H, N, Hg, Wg, HgWg;
   // Optional block mask: bit kb of word kb/32 of row (b, h, query block) selects key tile kb.
+  // Optional active-query subset: query rows are the tokens q_index[b * q_index_b_stride + i],
+  // i < Nq, gathered from q and scattered back into out / lse.
+  const int* q_index;          // nullptr: every token, in order
+  int Nq;                      // query rows per (b, h)
+  long long q_index_b_stride;  // entries between consecutive batches' lists (0: shared list)
+  const __nv_bfloat16* q;      // q itself, for the gather
   const uint32_t* kv_mask;     // nullptr: every key tile
   int mask_words;              // words per query block
   long long mask_bh_stride;    // words between consecutive (b, h) masks (0: one shared mask)
@@ -293,6 +299,43 @@ struct TileCursor {
   }
 };
 
+// Gather 128 query rows (tokens q_index[row_base + row]) straight from q, rotate each at its
+// own grid position and store them fp16 into a swizzled tile (rows past Nq, or with an index
+// outside [0, N), become zeros; bad indices also raise error bit 4).  Same thread-to-chunk
+// assignment as rope_tile.
+template <bool kLo>
+__device__ __forceinline__ float rope_gather_tile(const Params& p, const RopeLane& L, int t,
+                                                  uint8_t* tile, const int* idx, int row_base,
+                                                  int b, int h, const float2* __restrict__ tab,
+                                                  uint8_t* lo_tile = nullptr) {
+  float amax = 0.f;
+  const int c16 = t & 15;
+  const int rsub = t >> 4;
+  const uint32_t chunk_off = (c16 >> 3) * kHalfBytes + rsub * 128 + (((c16 & 7) ^ rsub) << 4);
+#pragma unroll 2
+  for (int it = 0; it < kBM / 8; ++it) {
+    const int i = row_base + it * 8 + rsub;
+    int n = i < p.Nq ? __ldg(idx + i) : -1;
+    if (i < p.Nq && (n < 0 || n >= p.N)) {
+      atomicOr(&g_error_word, 4u);
+      n = -1;
+    }
+    uint4 y = make_uint4(0u, 0u, 0u, 0u), ylo = y;
+    if (n >= 0) {
+      const int pt = n / p.HgWg;
+      const int rem = n - pt * p.HgWg;
+      const int ph = rem / p.Wg;
+      const int pw = rem - ph * p.Wg;
+      const uint4 x = __ldg(reinterpret_cast<const uint4*>(
+          p.q + ((static_cast<size_t>(b) * p.N + n) * p.H + h) * kD + c16 * 8));
+      y = rotate_chunk<kLo>(x, L, pt, ph, pw, tab, amax, &ylo);
+    }
+    *reinterpret_cast<uint4*>(tile + chunk_off + it * 1024) = y;
+    if (kLo) *reinterpret_cast<uint4*>(lo_tile + chunk_off + it * 1024) = ylo;
+  }
+  return amax;
+}
+
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -317,7 +360,8 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const int bh = blockIdx.x / p.n_qblk;
   const int b = bh / p.H;
   const int h = bh - b * p.H;
-  const int q0 = qblk * kRowsPerCta;
+  const int q0 = qblk * kRowsPerCta;               // first query row of this CTA
+  const int* q_idx = p.q_index ? p.q_index + static_cast<long long>(b) * p.q_index_b_stride : nullptr;
   const int nkv_all = (p.N + kBN - 1) / kBN;
   const uint32_t* mask_row =
       p.kv_mask ? p.kv_mask + (static_cast<long long>(bh) * p.mask_bh_stride +
@@ -372,7 +416,7 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       if (kSplit) tma_prefetch_desc(&tm_klo);
-      for (int i = 0; i < kQTiles; ++i) {
+      for (int i = 0; i < kQTiles && q_idx == nullptr; ++i) {   // a query subset is gathered by WG2
         const uint32_t bar = smem_addr(&ctl->q_full[i]);
         mbar_arrive_expect_tx(bar, kTileBytes);
         const uint32_t dst = sQ + i * kTileBytes;
@@ -410,7 +454,7 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
       }
       // Let every copy this thread started land before the CTA can retire.
-      for (int i = 0; i < kQTiles; ++i) drain_wait(smem_addr(&ctl->q_full[i]), 0);
+      for (int i = 0; i < kQTiles && q_idx == nullptr; ++i) drain_wait(smem_addr(&ctl->q_full[i]), 0);
       for (int s = 0; s < kKStages; ++s) {
         const int uses = k_issued > s ? (k_issued - 1 - s) / kKStages + 1 : 0;
         if (uses > 0) drain_wait(smem_addr(&ctl->k_full[s]), (uses - 1) & 1);
@@ -488,9 +532,15 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     bool ok = true;
     float amax = 0.f;
     for (int i = 0; i < kQTiles && ok; ++i) {
-      if (!(ok = mbar_wait(smem_addr(&ctl->q_full[i]), 0, abort_flag, kSiteQFull))) break;
-      amax = fmaxf(amax, rope_tile<kSplit>(p, L, t, smem + Lo::kOffQ + i * kTileBytes, q0 + i * kBM,
-                                           tab, smem + Lo::kOffQlo + i * kTileBytes));
+      if (q_idx) {
+        amax = fmaxf(amax, rope_gather_tile<kSplit>(p, L, t, smem + Lo::kOffQ + i * kTileBytes, q_idx,
+                                                    q0 + i * kBM, b, h, tab,
+                                                    smem + Lo::kOffQlo + i * kTileBytes));
+      } else {
+        if (!(ok = mbar_wait(smem_addr(&ctl->q_full[i]), 0, abort_flag, kSiteQFull))) break;
+        amax = fmaxf(amax, rope_tile<kSplit>(p, L, t, smem + Lo::kOffQ + i * kTileBytes, q0 + i * kBM,
+                                             tab, smem + Lo::kOffQlo + i * kTileBytes));
+      }
       fence_proxy_async_smem();
       mbar_arrive(smem_addr(&ctl->q_ready[i]));
     }
@@ -597,8 +647,13 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (ok) ok = mbar_wait(smem_addr(&ctl->o_final), 0, abort_flag, kSiteOFinal);
     if (ok) {
       tc_fence_after_sync();
-      const int n = q0 + qi * kBM + row;
-      const bool live = n < p.N;
+      const int i_row = q0 + qi * kBM + row;            // query row
+      int n = i_row;                                    // its token
+      bool live = i_row < p.Nq;
+      if (q_idx) {
+        n = live ? __ldg(q_idx + i_row) : 0;
+        live = live && n >= 0 && n < p.N;
+      }
       // A query block whose mask selects no key tile has no keys: out = 0, lse = -inf.
       const bool empty = nkv == 0;
       const float inv_l = empty ? 0.f : 1.f / l_run;
@@ -670,11 +725,15 @@ void fill_params(const Problem& pr, Params* p) {
   p->off_h = pr.T * pr.half_t;
   p->off_w = p->off_h + pr.Hg * pr.half_h;
   p->table_entries = pr.table_entries;
-  p->n_qblk = (pr.N + kRowsPerCta - 1) / kRowsPerCta;
   p->scale_log2 = pr.scale * 1.4426950408889634f;
   p->table = pr.table;
   p->out = static_cast<__nv_bfloat16*>(pr.out);
   p->lse = pr.lse;
+  p->q_index = pr.q_index;
+  p->Nq = pr.q_index ? pr.Nq : pr.N;
+  p->q_index_b_stride = pr.q_index_b_stride;
+  p->q = static_cast<const __nv_bfloat16*>(pr.q);
+  p->n_qblk = (p->Nq + kRowsPerCta - 1) / kRowsPerCta;
   p->kv_mask = pr.kv_mask;
   p->mask_words = pr.mask_words;
   p->mask_bh_stride = pr.mask_bh_stride;

@@ -198,7 +198,8 @@ extern "C" {
 static vdx_status attn_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
                             int B, int H, int T, int Hgrid, int Wgrid, int d, int sec_t, int sec_h,
                             int sec_w, double theta, float scale, const vdx_attn_options* opt,
-                            const uint32_t* block_mask, int mask_per_head, void* stream) {
+                            const uint32_t* block_mask, int mask_per_head, void* stream,
+                            const int32_t* q_index = nullptr, int Nq = 0, int index_per_batch = 0) {
   t_last_error.clear();
   if (d != 128) return fail(VDX_ERR_UNSUPPORTED, "bf16 path supports head_dim 128 only (got %d)", d);
   const int mode = opt ? opt->k_rope : VDX_K_ROPE_DEFAULT;
@@ -215,6 +216,13 @@ static vdx_status attn_bf16(const void* q, const void* k, const void* v, void* o
   vdx_status s = prepare(q, k, v, out, lse, B, H, T, Hgrid, Wgrid, d, sec_t, sec_h, sec_w, theta,
                          scale, 2, &p);
   if (s != VDX_OK) return s;
+  if (q_index) {
+    if (reinterpret_cast<uintptr_t>(q_index) & 3)
+      return fail(VDX_ERR_ALIGN, "q_index is not 4-byte aligned");
+    p.q_index = q_index;
+    p.Nq = Nq;
+    p.q_index_b_stride = index_per_batch ? Nq : 0;
+  }
   if (block_mask) {
     if (reinterpret_cast<uintptr_t>(block_mask) & 3)
       return fail(VDX_ERR_ALIGN, "block_mask is not 4-byte aligned");
@@ -283,6 +291,23 @@ vdx_status vdx_rope3d_attn_sparse(const void* q, const void* k, const void* v, v
   }
   return attn_bf16(q, k, v, out, lse, B, H, T, Hgrid, Wgrid, d, sec_t, sec_h, sec_w, theta, scale,
                    opt, block_mask, mask_per_head, stream);
+}
+
+vdx_status vdx_rope3d_attn_subset(const void* q, const void* k, const void* v, void* out,
+                                  float* lse, int B, int H, int T, int Hgrid, int Wgrid, int d,
+                                  int sec_t, int sec_h, int sec_w, double theta, float scale,
+                                  const int32_t* q_index, int Nq, int index_per_batch,
+                                  const vdx_attn_options* opt, void* stream) {
+  if (!q_index || Nq < 0) {
+    t_last_error.clear();
+    return fail(VDX_ERR_ARG, "q_index must be non-NULL and Nq >= 0");
+  }
+  if (Nq == 0) {
+    t_last_error.clear();
+    return VDX_OK;
+  }
+  return attn_bf16(q, k, v, out, lse, B, H, T, Hgrid, Wgrid, d, sec_t, sec_h, sec_w, theta, scale,
+                   opt, nullptr, 0, stream, q_index, Nq, index_per_batch);
 }
 
 int vdx_rope3d_block_mask_words(int T, int Hgrid, int Wgrid) {
@@ -378,6 +403,8 @@ vdx_status vdx_sync_check(void* stream) {
   if (word & 2u)
     return fail(VDX_ERR_RANGE, "a rotated q/k value exceeded the fp16 operand range (|x| > 65504); "
                                "it was clamped and the result is inexact");
+  if (word & 4u)
+    return fail(VDX_ERR_ARG, "a q_index entry was outside [0, N); those rows were skipped");
   return VDX_OK;
 }
 

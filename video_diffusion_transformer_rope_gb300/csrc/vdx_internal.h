@@ -24,6 +24,10 @@ struct Problem {
   int table_entries;
   // Optional block mask (device): row (b, h, query block of 256) at word offset
   // (b*H + h) * mask_bh_stride + qblock * mask_words; bit kb of word kb/32 selects key tile kb.
+  // Optional active-query subset: rows are tokens q_index[b * q_index_b_stride + i], i < Nq.
+  const int* q_index = nullptr;
+  int Nq = 0;
+  long long q_index_b_stride = 0;
   const uint32_t* kv_mask = nullptr;
   int mask_words = 0;
   long long mask_bh_stride = 0;
