@@ -72,6 +72,10 @@ typedef struct vdx_attn_options {
                                cudaMalloc on first need; shared by every call on that device, so
                                calls that may overlap on different streams should pass their own) */
   size_t workspace_bytes;   /* size of `workspace` in bytes                                      */
+  int test_withhold_kv;     /* testing only, keep 0: the kernel's copy engine issues no K/V tile,
+                               so every pipeline wait runs out (after about 1 s); the kernel then
+                               stops cleanly and vdx_sync_check reports VDX_ERR_TIMEOUT (this is
+                               how the failure path is exercised without faulting the GPU)    */
 } vdx_attn_options;
 
 /* bf16 path, tcgen05 tensor cores.  q, k, v, out: __nv_bfloat16 [B, N, H, d]; d must be 128.

@@ -1,0 +1,47 @@
+"""bench.py's multi-rank logic on CPU: two gloo ranks (replicas), the step time is the slowest
+rank's and the job value sums the replicas' work over it."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank(rank, ws, port, results):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(ws), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    wsz, r, local = bench._dist()
+    assert (wsz, r, local) == (ws, rank, rank)
+    ms = 100.0 + 25.0 * rank                      # rank 1 is the slower replica
+    worst = bench.reduce_max_over_ranks(ms, ws, torch.device("cpu"))
+    results[rank] = (worst, bench.job_tflops(2.341e14, worst, ws))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_replicas_aggregate():
+    ws = 2
+    port = _free_port()
+    mgr = mp.Manager()
+    results = mgr.dict()
+    mp.spawn(_rank, args=(ws, port, results), nprocs=ws, join=True)
+    assert results[0][0] == results[1][0] == 125.0
+    assert results[0][1] == pytest.approx(2 * 2.341e14 / 0.125 / 1e12)
+
+
+def test_single_rank_is_identity():
+    assert bench.reduce_max_over_ranks(3.5, 1, torch.device("cpu")) == 3.5
+    assert bench.job_tflops(1e12, 1000.0, 1) == pytest.approx(1.0)

@@ -76,12 +76,12 @@ def test_workspace_bytes(L):
 
 
 def test_ex_rejects_bad_options(L):
-    opt = _binding.AttnOptions(7, 0, None, 0)
+    opt = _binding.AttnOptions(7, 0, None, 0, 0)
     r = L.vdx_rope3d_attn_ex(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + (1 << 32)),
                              ctypes.c_void_p(FAKE + (2 << 32)), ctypes.c_void_p(FAKE + (3 << 32)),
                              None, 1, 2, 2, 3, 4, 128, 0, 0, 0, 10000.0, 0.0, ctypes.byref(opt), None)
     assert r == _binding.VDX_ERR_ARG and "k_rope" in L.vdx_last_error().decode()
-    opt = _binding.AttnOptions(_binding.K_ROPE_FUSED, _binding.QK_SPLIT, None, 0)
+    opt = _binding.AttnOptions(_binding.K_ROPE_FUSED, _binding.QK_SPLIT, None, 0, 0)
     r = L.vdx_rope3d_attn_ex(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + (1 << 32)),
                              ctypes.c_void_p(FAKE + (2 << 32)), ctypes.c_void_p(FAKE + (3 << 32)),
                              None, 1, 2, 2, 3, 4, 128, 0, 0, 0, 10000.0, 0.0, ctypes.byref(opt), None)

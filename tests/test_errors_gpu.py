@@ -33,3 +33,29 @@ def test_bad_arguments_raise_before_launch():
         vdx.rope3d_attn(q, q.clone(), q.clone(), (1, 2, 4), out=q)
     assert ei.value.status == 1
     vdx.sync_check()
+
+
+def test_pipeline_wait_timeout_is_reported_and_context_stays_usable():
+    # The producer withholds every K/V tile: the MMA and softmax waits run out after ~1 s, the
+    # kernel stops cleanly (TMEM freed, its own copies drained), and the status says so.
+    import ctypes
+    from video_diffusion_transformer_rope_gb300 import _binding
+    w = dataclasses.replace(configs.WAN13B_480P, B=1, H=1, T=1, Hg=2, Wg=64, seed=32)
+    q, k, v = (t.cuda() for t in synth.make_qkv(w))
+    out = torch.empty_like(q)
+    opt = _binding.AttnOptions(vdx.K_ROPE_PREPASS, vdx.QK_FP16, None, 0, 1)
+    L = vdx.lib()
+    st = L.vdx_rope3d_attn_ex(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                              ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()), None,
+                              1, 1, 1, 2, 64, 128, 0, 0, 0, 10000.0, 0.0, ctypes.byref(opt), None)
+    assert st == 0
+    with pytest.raises(vdx.VdxError) as ei:
+        vdx.sync_check()
+    assert ei.value.status == _binding.VDX_ERR_TIMEOUT
+    # the next ordinary call on the same context is correct
+    import oracle.fp64 as O
+    import numpy as np
+    o2, l2 = vdx.rope3d_attn(q, k, v, (1, 2, 64))
+    vdx.sync_check()
+    ref_o, _ = O.rope3d_attention(q, k, v, (1, 2, 64))
+    assert np.abs(o2.double().cpu().numpy() - ref_o).max() <= 2e-2

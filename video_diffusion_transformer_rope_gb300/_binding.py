@@ -22,7 +22,8 @@ QK_FP16, QK_SPLIT = 0, 1
 class AttnOptions(ctypes.Structure):
     """vdx_attn_options (include/vdx.h)."""
     _fields_ = [("k_rope", ctypes.c_int), ("qk_precision", ctypes.c_int),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("test_withhold_kv", ctypes.c_int)]
 # name -> (restype, argtypes); mirrors include/vdx.h
 SIGNATURES = {
     "vdx_rope3d_attn": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f, _p]),

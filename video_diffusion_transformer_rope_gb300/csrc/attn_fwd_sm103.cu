@@ -117,6 +117,7 @@ struct Params {
   int Nq;                      // query rows per (b, h)
   long long q_index_b_stride;  // entries between consecutive batches' lists (0: shared list)
   const __nv_bfloat16* q;      // q itself, for the gather
+  int withhold_kv;             // testing only: the producer issues no K/V copy (waits expire)
   const uint32_t* kv_mask;     // nullptr: every key tile
   int mask_words;              // words per query block
   long long mask_bh_stride;    // words between consecutive (b, h) masks (0: one shared mask)
@@ -424,7 +425,7 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tma_load_4d(dst + kHalfBytes, &tm_q, bar, 64, h, q0 + i * kBM, b);
       }
       int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < nkv; ++j) {
+      for (int j = 0; j < nkv && !p.withhold_kv; ++j) {
         const int kt = cur.next();          // key tile of step j
         const int ks = j % kKStages, ku = j / kKStages;
         if (ku > 0 && !mbar_wait(smem_addr(&ctl->k_empty[ks]), (ku - 1) & 1, abort_flag, kSiteKEmpty))
@@ -734,6 +735,7 @@ void fill_params(const Problem& pr, Params* p) {
   p->q_index_b_stride = pr.q_index_b_stride;
   p->q = static_cast<const __nv_bfloat16*>(pr.q);
   p->n_qblk = (p->Nq + kRowsPerCta - 1) / kRowsPerCta;
+  p->withhold_kv = pr.withhold_kv;
   p->kv_mask = pr.kv_mask;
   p->mask_words = pr.mask_words;
   p->mask_bh_stride = pr.mask_bh_stride;

@@ -216,6 +216,7 @@ static vdx_status attn_bf16(const void* q, const void* k, const void* v, void* o
   vdx_status s = prepare(q, k, v, out, lse, B, H, T, Hgrid, Wgrid, d, sec_t, sec_h, sec_w, theta,
                          scale, 2, &p);
   if (s != VDX_OK) return s;
+  p.withhold_kv = (opt && opt->test_withhold_kv) ? 1 : 0;
   if (q_index) {
     if (reinterpret_cast<uintptr_t>(q_index) & 3)
       return fail(VDX_ERR_ALIGN, "q_index is not 4-byte aligned");

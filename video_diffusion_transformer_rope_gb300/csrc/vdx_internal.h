@@ -28,6 +28,7 @@ struct Problem {
   const int* q_index = nullptr;
   int Nq = 0;
   long long q_index_b_stride = 0;
+  int withhold_kv = 0;        // testing only (vdx_attn_options.test_withhold_kv)
   const uint32_t* kv_mask = nullptr;
   int mask_words = 0;
   long long mask_bh_stride = 0;
