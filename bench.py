@@ -43,9 +43,16 @@ def _peaks():
 
 
 def _source_hash():
+    """Hash of the attention kernel's code with comments and blank space removed, so that a
+    stored DRAM-traffic figure stays attached to the code it was measured on."""
     import hashlib
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    import re
+    with open(KERNEL_SRC) as f:
+        src = f.read()
+    src = re.sub(r"//[^\n]*", "", src)
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = "\n".join(line.strip() for line in src.splitlines() if line.strip())
+    return hashlib.sha256(src.encode()).hexdigest()[:16]
 
 
 def _traffic_per_launch(workload):

@@ -8,15 +8,17 @@
 // 8x finer than bf16) for the QK^T product; P and V enter the PV product as bf16.
 //
 // One CTA owns 256 query rows (two 128-row Q tiles) of one (batch, head) and streams every
-// 128-key K/V tile of that head.  Warp roles (one warpgroup each, registers rebalanced with
-// setmaxnreg once the roles split):
+// 128-key K/V tile of that head (or, with a block mask, the tiles its mask row selects).
+// Warp roles (one warpgroup each, registers rebalanced with setmaxnreg once the roles split):
 //
 //   WG0  warps 0-3   softmax + epilogue for Q tile 0 (thread = query row = TMEM lane)
 //   WG1  warps 4-7   softmax + epilogue for Q tile 1
 //   WG2  warps 8-11  RoPE: rotate the Q tiles in shared memory as they land (bf16 -> fp16,
-//                    in place); in the fused-K mode also every K tile
+//                    in place), or gather + rotate a query subset straight from global
+//                    memory; in the fused-K mode also every K tile
 //   WG3  warp 12     TMA producer: Q tiles once, then K/V tiles through the rings
-//        warp 13     tcgen05 MMA issuer (one thread) and TMEM owner; warps 14-15 idle
+//        warp 13     tcgen05 MMA issuer (the whole warp runs the loop, one elected lane
+//                    issues) and TMEM owner; warps 14-15 idle
 //
 // K modes.  Prepass (default): a separate kernel rotates K once per token into an fp16
 // workspace and the attention kernel streams that, so no K rotation sits in the hot loop.
