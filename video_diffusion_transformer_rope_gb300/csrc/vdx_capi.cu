@@ -20,6 +20,8 @@
 #include <tuple>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "vdx.h"
 #include "vdx_internal.h"
 
@@ -195,11 +197,18 @@ void set_last_error(const char* message) { t_last_error = message; }
 
 extern "C" {
 
+// NVTX range over a host call (shows up in profilers that record NVTX; free otherwise).
+struct NvtxScope {
+  explicit NvtxScope(const char* name) { nvtxRangePushA(name); }
+  ~NvtxScope() { nvtxRangePop(); }
+};
+
 static vdx_status attn_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
                             int B, int H, int T, int Hgrid, int Wgrid, int d, int sec_t, int sec_h,
                             int sec_w, double theta, float scale, const vdx_attn_options* opt,
                             const uint32_t* block_mask, int mask_per_head, void* stream,
                             const int32_t* q_index = nullptr, int Nq = 0, int index_per_batch = 0) {
+  NvtxScope nvtx(block_mask ? "vdx_rope3d_attn_sparse" : (q_index ? "vdx_rope3d_attn_subset" : "vdx_rope3d_attn"));
   t_last_error.clear();
   if (d != 128) return fail(VDX_ERR_UNSUPPORTED, "bf16 path supports head_dim 128 only (got %d)", d);
   const int mode = opt ? opt->k_rope : VDX_K_ROPE_DEFAULT;
@@ -380,6 +389,7 @@ vdx_status vdx_rope3d_attn_f32(const float* q, const float* k, const float* v, f
                                float* lse, int B, int H, int T, int Hgrid, int Wgrid, int d,
                                int sec_t, int sec_h, int sec_w, double theta, float scale,
                                void* stream) {
+  NvtxScope nvtx("vdx_rope3d_attn_f32");
   t_last_error.clear();
   if (d != 64 && d != 128)
     return fail(VDX_ERR_UNSUPPORTED, "fp32 path supports head_dim 64 or 128 (got %d)", d);
