@@ -88,3 +88,26 @@ def test_out_of_range_index_is_skipped_and_reported():
     assert not torch.all(out[0, 5] == 3.0) and not torch.all(out[0, 7] == 3.0)
     keep = [i for i in range(w.N) if i not in (5, 7)]
     assert torch.all(out[0, keep] == 3.0)
+
+
+def test_ulysses_single_rank_on_gpu_equals_direct_call():
+    # One NCCL rank on this GPU: the exchanges are identities and the library does the work.
+    import os
+    import socket
+    import torch.distributed as dist
+    from video_diffusion_transformer_rope_gb300.ulysses import ulysses_rope3d_attn
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("nccl", rank=0, world_size=1, device_id=torch.device("cuda", 0))
+    try:
+        w = dataclasses.replace(configs.WAN13B_480P, B=2, H=4, T=2, Hg=8, Wg=20, seed=65)
+        q, k, v = (t.cuda() for t in synth.make_qkv(w))
+        o1, l1 = ulysses_rope3d_attn(q, k, v, (w.T, w.Hg, w.Wg))
+        o2, l2 = vdx.rope3d_attn(q, k, v, (w.T, w.Hg, w.Wg))
+        vdx.sync_check()
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    finally:
+        dist.destroy_process_group()
