@@ -430,6 +430,10 @@ def main():
                     help="K rotated once by a prepass kernel (default) or per tile inside the "
                          "attention kernel")
     args = ap.parse_args()
+    ws_env = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != ws_env:
+        ap.error(f"--gpus {args.gpus} but {ws_env} process(es) were launched: run N > 1 under "
+                 "torchrun (one process per GPU)")
     w = configs.BY_NAME[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

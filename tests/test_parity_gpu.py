@@ -188,3 +188,27 @@ def test_full_size_fused_k_mode_sampled():
     mx, mean, lerr = _sampled_compare(w, k_rope=vdx.K_ROPE_FUSED)
     print(f"{w.name}: out max {mx:.3e} mean {mean:.3e} lse max {lerr:.3e}")
     assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
+
+
+@pytest.mark.parametrize("sections,theta", [((128, 0, 0), 10000.0), ((0, 64, 64), 10000.0),
+                                            ((44, 42, 42), 1.0e6), ((2, 2, 124), 2.0)])
+def test_bf16_degenerate_sections_and_theta(sections, theta):
+    w = dataclasses.replace(configs.WAN13B_480P, B=1, H=2, T=3, Hg=7, Wg=11, seed=28,
+                            sections=sections, theta=theta)
+    mx, mean, lerr = _full_compare(w)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
+
+
+@pytest.mark.parametrize("which", ["k", "q"])
+def test_bf16_uniform_attention_closed_form(which):
+    # Zero keys (or zero queries) make every logit 0: out = mean of V, lse = ln N.
+    w = dataclasses.replace(configs.WAN13B_480P, B=2, H=2, T=2, Hg=9, Wg=21, seed=29)
+    q, k, v = (t.cuda() for t in synth.make_qkv(w))
+    if which == "k":
+        k = torch.zeros_like(k)
+    else:
+        q = torch.zeros_like(q)
+    out, lse = _run(w, q, k, v)
+    mean_v = v.double().mean(dim=1, keepdim=True)
+    assert (out.double() - mean_v).abs().max().item() <= 4e-3      # bf16 P = 1 exactly; bf16 out
+    assert (lse.double() - np.log(w.N)).abs().max().item() <= 1e-5
