@@ -79,9 +79,10 @@ typedef struct vdx_attn_options {
 } vdx_attn_options;
 
 /* bf16 path, tcgen05 tensor cores.  q, k, v, out: __nv_bfloat16 [B, N, H, d]; d must be 128.
- * Arithmetic: rotation in fp32; rotated q and k rounded to fp16 for QK^T (so |q|, |k| must stay
- * below ~46000, else values are clamped and vdx_sync_check reports VDX_ERR_RANGE); scores,
- * softmax statistics and the output accumulator in fp32; P and v enter PV as bf16.
+ * Arithmetic: rotation in fp32; rotated k, and rotated q multiplied by scale*log2(e), rounded
+ * to fp16 for QK^T (so |k| and |q|*scale*log2(e) must stay below ~46000, else values are
+ * clamped and vdx_sync_check reports VDX_ERR_RANGE); scores (in log2 units), softmax
+ * statistics and the output accumulator in fp32; P and v enter PV as bf16.
  * sec_t/sec_h/sec_w: even, sum to d; all three 0 selects d - 4*(d/6), 2*(d/6), 2*(d/6)
  * (44/42/42 at d = 128).  scale <= 0 selects 1/sqrt(d).  theta > 0 (10000 for Wan).
  * out must not overlap q, k or v.  B, H, T, Hgrid, Wgrid >= 1. */

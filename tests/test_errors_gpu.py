@@ -13,11 +13,23 @@ pytestmark = pytest.mark.gpu
 def test_fp16_range_flag_and_clear():
     w = dataclasses.replace(configs.WAN13B_480P, B=1, H=1, T=1, Hg=2, Wg=64, seed=31)
     q, k, v = (t.cuda() for t in synth.make_qkv(w))
-    q[0, 5, 0, 3] = 70000.0          # bf16 70144: above the fp16 maximum 65504 at any angle
+    # Token 5 sits at t = 0, so channel pair (2, 3) (a t-axis pair) is not rotated.
+    # K is stored as rotated: bf16 70144 is above the fp16 maximum 65504.
+    k[0, 5, 0, 3] = 70000.0
     vdx.rope3d_attn(q, k, v, (1, 2, 64))
     with pytest.raises(vdx.VdxError) as ei:
         vdx.sync_check()
     assert ei.value.status == 6 and "fp16" in str(ei.value)
+    k[0, 5, 0, 3] = 1.0
+    # Q is stored multiplied by scale*log2(e) = 0.1275: 70000 fits, 600000 (bf16 599040) does not.
+    q[0, 5, 0, 3] = 70000.0
+    vdx.rope3d_attn(q, k, v, (1, 2, 64))
+    vdx.sync_check()
+    q[0, 5, 0, 3] = 600000.0
+    vdx.rope3d_attn(q, k, v, (1, 2, 64))
+    with pytest.raises(vdx.VdxError) as ei:
+        vdx.sync_check()
+    assert ei.value.status == 6
     # the word is cleared by the read; an in-range call afterwards is clean
     q[0, 5, 0, 3] = 1.0
     vdx.rope3d_attn(q, k, v, (1, 2, 64))

@@ -35,8 +35,9 @@
 //     S0(j) = Q0 K_j^T ;  O1 += P1(j-1) V_{j-1} ;  S1(j) = Q1 K_j^T ;  O0 += P0(j) V_j
 // so softmax of one Q tile overlaps the tensor-core work of the other.  Completion of S_i(j)
 // implies completion of every earlier MMA, so O_i may be rescaled as soon as S_i(j) is seen.
-// The online softmax works in the log2 domain (exp2 with scale*log2(e) folded into one FMA)
-// and only rescales O when a row maximum grows by more than 8 (a factor 256): P <= 256.
+// The online softmax works in the log2 domain: the rotated Q tiles are stored already
+// multiplied by scale*log2(e), so S comes out of the MMA in log2 units and p = 2^(s - m).
+// O is rescaled only when a row maximum grows by more than 8 (a factor 256): P <= 256.
 //
 // Shared memory: Q 2x32 KB, K ring, V ring (32 KB per stage), each tile stored as two
 // 128-row x 128-byte halves in the 128-byte-swizzled layout TMA writes; then (fused mode,
@@ -212,18 +213,21 @@ __device__ __forceinline__ RopeLane make_rope_lane(int c16, int half_t, int half
   return L;
 }
 
-// Rotate the 4 pairs of one 16-byte chunk (bf16 in) of a token at grid position (pt,ph,pw);
-// returns the fp16 result and folds |rotated| into amax.
+// Rotate the 4 pairs of one 16-byte chunk (bf16 in) of a token at grid position (pt,ph,pw)
+// and multiply by qs (scale*log2(e) for Q, 1 for K); returns the fp16 result and folds
+// |result| into amax.
 template <bool kLo>
 __device__ __forceinline__ uint4 rotate_chunk(uint4 x, const RopeLane& L, int pt, int ph, int pw,
                                               const float2* __restrict__ tab, float& amax,
-                                              uint4* lo_out = nullptr) {
+                                              uint4* lo_out = nullptr, float qs = 1.f) {
   uint32_t w[4] = {x.x, x.y, x.z, x.w};
   uint32_t wl[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const int pos = L.axis[e] == 0 ? pt : (L.axis[e] == 1 ? ph : pw);
-    const float2 cs = tab[L.tab_base[e] + pos * L.tab_stride[e]];
+    float2 cs = tab[L.tab_base[e] + pos * L.tab_stride[e]];
+    cs.x *= qs;
+    cs.y *= qs;
     const float x0 = __uint_as_float(w[e] << 16);
     const float x1 = __uint_as_float(w[e] & 0xffff0000u);
     const float y0 = fmaf(x0, cs.x, -x1 * cs.y);
@@ -244,7 +248,7 @@ __device__ __forceinline__ uint4 rotate_chunk(uint4 x, const RopeLane& L, int pt
 // 16-byte bank groups.
 template <bool kLo>
 __device__ __forceinline__ float rope_tile(const Params& p, const RopeLane& L, int t, uint8_t* tile,
-                                           int n_first, const float2* __restrict__ tab,
+                                           int n_first, const float2* __restrict__ tab, float qs,
                                            uint8_t* lo_tile = nullptr) {
   float amax = 0.f;
   const int c16 = t & 15;
@@ -261,7 +265,7 @@ __device__ __forceinline__ float rope_tile(const Params& p, const RopeLane& L, i
     if (n >= p.N) break;
     uint4* ptr = reinterpret_cast<uint4*>(tile + chunk_off + it * 1024);
     *ptr = rotate_chunk<kLo>(*ptr, L, pt, ph, pw, tab, amax,
-                             kLo ? reinterpret_cast<uint4*>(lo_tile + chunk_off + it * 1024) : nullptr);
+                             kLo ? reinterpret_cast<uint4*>(lo_tile + chunk_off + it * 1024) : nullptr, qs);
     n += 8;
     pw += 8;
     while (pw >= p.Wg) { pw -= p.Wg; ++ph; }
@@ -309,7 +313,7 @@ struct TileCursor {
 template <bool kLo>
 __device__ __forceinline__ float rope_gather_tile(const Params& p, const RopeLane& L, int t,
                                                   uint8_t* tile, const int* idx, int row_base,
-                                                  int b, int h, const float2* __restrict__ tab,
+                                                  int b, int h, const float2* __restrict__ tab, float qs,
                                                   uint8_t* lo_tile = nullptr) {
   float amax = 0.f;
   const int c16 = t & 15;
@@ -331,7 +335,7 @@ __device__ __forceinline__ float rope_gather_tile(const Params& p, const RopeLan
       const int pw = rem - ph * p.Wg;
       const uint4 x = __ldg(reinterpret_cast<const uint4*>(
           p.q + ((static_cast<size_t>(b) * p.N + n) * p.H + h) * kD + c16 * 8));
-      y = rotate_chunk<kLo>(x, L, pt, ph, pw, tab, amax, &ylo);
+      y = rotate_chunk<kLo>(x, L, pt, ph, pw, tab, amax, &ylo, qs);
     }
     *reinterpret_cast<uint4*>(tile + chunk_off + it * 1024) = y;
     if (kLo) *reinterpret_cast<uint4*>(lo_tile + chunk_off + it * 1024) = ylo;
@@ -476,12 +480,21 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 mbar_wait(smem_addr(&ctl->q_ready[1]), 0, abort_flag, kSiteQReady);
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after_sync();
+      // K tile j is ready: waited for at the top of step j with a one-stage ring (split mode:
+      // K(j+1) lands only after S1(j) frees the stage), else before PV0(j-1) so that S0(j)
+      // follows PV0(j-1) without a barrier wait in between.
+      auto k_wait = [&](int jj) {
+        const int kss = jj % kKStages;
+        const uint32_t kbar = kFusedK ? smem_addr(&ctl->k_ready[kss]) : smem_addr(&ctl->k_full[kss]);
+        return mbar_wait(kbar, (jj / kKStages) & 1, abort_flag, kFusedK ? kSiteKReady : kSiteKFull);
+      };
+      if (!kSplit && ok && nkv > 0) ok = __all_sync(0xffffffffu, k_wait(0));
       for (int j = 0; ok && j < nkv; ++j) {
         const int ks = j % kKStages;
-        const uint32_t kbar = kFusedK ? smem_addr(&ctl->k_ready[ks]) : smem_addr(&ctl->k_full[ks]);
-        ok = __all_sync(0xffffffffu, mbar_wait(kbar, (j / kKStages) & 1, abort_flag,
-                                               kFusedK ? kSiteKReady : kSiteKFull));
-        if (!ok) break;
+        if (kSplit) {
+          ok = __all_sync(0xffffffffu, k_wait(j));
+          if (!ok) break;
+        }
         tc_fence_after_sync();
         const uint32_t kt = sK + ks * Lo::kKStageBytes;
         const uint32_t sQlo = smem_addr(smem + Lo::kOffQlo);
@@ -510,6 +523,7 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int vs = j % kVStages;
         ok = __all_sync(0xffffffffu,
                         mbar_wait(smem_addr(&ctl->v_full[vs]), (j / kVStages) & 1, abort_flag, kSiteVFull) &&
+                        (kSplit || j + 1 >= nkv || k_wait(j + 1)) &&
                         mbar_wait(smem_addr(&ctl->p_ready[0]), j & 1, abort_flag, kSitePReady));
         if (!ok) break;
         tc_fence_after_sync();
@@ -537,12 +551,12 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     for (int i = 0; i < kQTiles && ok; ++i) {
       if (q_idx) {
         amax = fmaxf(amax, rope_gather_tile<kSplit>(p, L, t, smem + Lo::kOffQ + i * kTileBytes, q_idx,
-                                                    q0 + i * kBM, b, h, tab,
+                                                    q0 + i * kBM, b, h, tab, p.scale_log2,
                                                     smem + Lo::kOffQlo + i * kTileBytes));
       } else {
         if (!(ok = mbar_wait(smem_addr(&ctl->q_full[i]), 0, abort_flag, kSiteQFull))) break;
         amax = fmaxf(amax, rope_tile<kSplit>(p, L, t, smem + Lo::kOffQ + i * kTileBytes, q0 + i * kBM,
-                                             tab, smem + Lo::kOffQlo + i * kTileBytes));
+                                             tab, p.scale_log2, smem + Lo::kOffQlo + i * kTileBytes));
       }
       fence_proxy_async_smem();
       mbar_arrive(smem_addr(&ctl->q_ready[i]));
@@ -553,7 +567,7 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int ks = j % kKStages;
         if (!(ok = mbar_wait(smem_addr(&ctl->k_full[ks]), (j / kKStages) & 1, abort_flag, kSiteKFull)))
           break;
-        amax = fmaxf(amax, rope_tile<false>(p, L, t, smem + Lo::kOffK + ks * Lo::kKStageBytes, kt * kBN, tab));
+        amax = fmaxf(amax, rope_tile<false>(p, L, t, smem + Lo::kOffK + ks * Lo::kKStageBytes, kt * kBN, tab, 1.f));
         fence_proxy_async_smem();
         mbar_arrive(smem_addr(&ctl->k_ready[ks]));
       }
@@ -567,8 +581,6 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t lane_bits = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_bits + 128 * qi;
     const uint32_t tO = tmem + lane_bits + 256 + 128 * qi;
-    const float c = p.scale_log2;
-    const uint64_t c2 = f32x2(c, c);
     float m_run = -INFINITY;
     float l_run = 0.f;
     bool ok = true;
@@ -601,7 +613,7 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       for (int i = 0; i < 5; ++i) mx16[i] = fmax3(mx16[i], mx16[i + 5], mx16[i + 10]);
       const float mx = fmax3(fmax3(mx16[0], mx16[1], mx16[2]), fmax3(mx16[3], mx16[4], mx16[15]),
                              -INFINITY);
-      const float m_new = fmaxf(m_run, mx * c);
+      const float m_new = fmaxf(m_run, mx);
       const bool resc = m_new > m_run + 8.0f;
       float alpha = 1.f;
       if (resc) {
@@ -615,7 +627,7 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       uint32_t pk[64];
 #pragma unroll
       for (int e2 = 0; e2 < 64; ++e2) {
-        const uint64_t a = ffma2(f32x2(__uint_as_float(s[2 * e2]), __uint_as_float(s[2 * e2 + 1])), c2, negm2);
+        const uint64_t a = fadd2(f32x2(__uint_as_float(s[2 * e2]), __uint_as_float(s[2 * e2 + 1])), negm2);
         float a0, a1;
         f32x2_split(a, a0, a1);
         const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
