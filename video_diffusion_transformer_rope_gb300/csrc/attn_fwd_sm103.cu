@@ -37,7 +37,9 @@
 // implies completion of every earlier MMA, so O_i may be rescaled as soon as S_i(j) is seen.
 // The online softmax works in the log2 domain: the rotated Q tiles are stored already
 // multiplied by scale*log2(e), so S comes out of the MMA in log2 units and p = 2^(s - m).
-// O is rescaled only when a row maximum grows by more than 8 (a factor 256): P <= 256.
+// Each tile's exponentials are taken against the running maximum m and kept when the row
+// sum shows every p <= 256; only otherwise (the first tile, or scores that rose) is the tile
+// maximum computed, m moved there, l and O rescaled and the row redone.
 //
 // Shared memory: Q 2x32 KB, K ring, V ring (32 KB per stage), each tile stored as two
 // 128-row x 128-byte halves in the 128-byte-swizzled layout TMA writes; then (fused mode,
@@ -139,6 +141,44 @@ struct Params {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Row maximum of one 128-column score row: 16 independent 3-input max chains, then a short tree.
+__device__ __forceinline__ float row_max128(const uint32_t (&s)[128]) {
+  float mx16[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    mx16[i] = fmax3(__uint_as_float(s[i]), __uint_as_float(s[i + 16]), __uint_as_float(s[i + 32]));
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    mx16[i] = fmax3(mx16[i], __uint_as_float(s[i + 48]), __uint_as_float(s[i + 64]));
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    mx16[i] = fmax3(mx16[i], __uint_as_float(s[i + 80]), __uint_as_float(s[i + 96]));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) mx16[i] = fmaxf(mx16[i], __uint_as_float(s[i + 112]));
+#pragma unroll
+  for (int i = 0; i < 5; ++i) mx16[i] = fmax3(mx16[i], mx16[i + 5], mx16[i + 10]);
+  return fmax3(fmax3(mx16[0], mx16[1], mx16[2]), fmax3(mx16[3], mx16[4], mx16[15]), -INFINITY);
+}
+
+// p = 2^(s - m) for one 128-column row (scores in log2 units), packed to bf16 pairs in pk;
+// returns the row sum of the fp32 p (four packed accumulators).
+__device__ __forceinline__ float exp_row128(const uint32_t (&s)[128], float m, uint32_t (&pk)[64]) {
+  const uint64_t negm2 = f32x2(-m, -m);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int e2 = 0; e2 < 64; ++e2) {
+    const uint64_t a = fadd2(f32x2(__uint_as_float(s[2 * e2]), __uint_as_float(s[2 * e2 + 1])), negm2);
+    float a0, a1;
+    f32x2_split(a, a0, a1);
+    const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+    acc[e2 & 3] = fadd2(acc[e2 & 3], f32x2(p0, p1));
+    pk[e2] = pack_bf16x2(p0, p1);
+  }
+  float l0, l1;
+  f32x2_split(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), l0, l1);
+  return l0 + l1;
 }
 
 // Round to fp16 with saturation to +-65504 (no infinities); `lo` lands in the low half.
@@ -596,43 +636,30 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int e = 0; e < 128; ++e)
           if (e >= valid) s[e] = 0xff800000u;
       }
-      // row maximum: 16 independent 3-input max chains, then a short tree
-      float mx16[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        mx16[i] = fmax3(__uint_as_float(s[i]), __uint_as_float(s[i + 16]), __uint_as_float(s[i + 32]));
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        mx16[i] = fmax3(mx16[i], __uint_as_float(s[i + 48]), __uint_as_float(s[i + 64]));
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        mx16[i] = fmax3(mx16[i], __uint_as_float(s[i + 80]), __uint_as_float(s[i + 96]));
-#pragma unroll
-      for (int i = 0; i < 16; ++i) mx16[i] = fmaxf(mx16[i], __uint_as_float(s[i + 112]));
-#pragma unroll
-      for (int i = 0; i < 5; ++i) mx16[i] = fmax3(mx16[i], mx16[i + 5], mx16[i + 10]);
-      const float mx = fmax3(fmax3(mx16[0], mx16[1], mx16[2]), fmax3(mx16[3], mx16[4], mx16[15]),
-                             -INFINITY);
-      const float m_new = fmaxf(m_run, mx);
-      const bool resc = m_new > m_run + 8.0f;
-      float alpha = 1.f;
-      if (resc) {
-        alpha = ex2_approx(m_run - m_new);
-        l_run *= alpha;
-        m_run = m_new;
-      }
-      // p = 2^(s*c - m), packed in pairs; row sum in 4 packed accumulators
-      const uint64_t negm2 = f32x2(-m_run, -m_run);
-      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+      // Exponentials against the running maximum, kept when the row sum shows every p <= 256
+      // (P then stays within the range the accumulators are sized for).  Otherwise (the first
+      // tile, or a row whose scores rose) take the exact tile maximum, move the running
+      // maximum there, rescale l (and O below) and redo the row; S is still intact in TMEM
+      // because P has not been stored yet.
       uint32_t pk[64];
+      float l_tile = exp_row128(s, m_run, pk);
+      bool resc = false;
+      float alpha = 1.f;
+      if (__any_sync(0xffffffffu, !(l_tile <= 256.f))) {
+        tmem_ld128(tS, s);
+        if (valid < kBN) {
 #pragma unroll
-      for (int e2 = 0; e2 < 64; ++e2) {
-        const uint64_t a = fadd2(f32x2(__uint_as_float(s[2 * e2]), __uint_as_float(s[2 * e2 + 1])), negm2);
-        float a0, a1;
-        f32x2_split(a, a0, a1);
-        const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-        acc[e2 & 3] = fadd2(acc[e2 & 3], f32x2(p0, p1));
-        pk[e2] = pack_bf16x2(p0, p1);
+          for (int e = 0; e < 128; ++e)
+            if (e >= valid) s[e] = 0xff800000u;
+        }
+        const float m_new = fmaxf(m_run, row_max128(s));
+        resc = m_new > m_run;
+        if (resc) {
+          alpha = ex2_approx(m_run - m_new);
+          l_run *= alpha;
+          m_run = m_new;
+        }
+        l_tile = exp_row128(s, m_run, pk);
       }
       {
         uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
@@ -640,11 +667,7 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tmem_st32(tS, lo);
         tmem_st32(tS + 32, hi);
       }
-      const uint64_t acc01 = fadd2(acc[0], acc[1]);
-      const uint64_t acc23 = fadd2(acc[2], acc[3]);
-      float l0, l1;
-      f32x2_split(fadd2(acc01, acc23), l0, l1);
-      l_run += l0 + l1;
+      l_run += l_tile;
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
         uint32_t r[32];
 #pragma unroll 1
