@@ -67,7 +67,7 @@ typedef struct vdx_attn_options {
   int k_rope;               /* one of VDX_K_ROPE_*                                              */
   int qk_precision;         /* one of VDX_QK_*                                                  */
   void* workspace;          /* device scratch for the prepass, >= vdx_rope3d_workspace_bytes()
-                               bytes, 16-byte aligned, not overlapping q/k/v/out; NULL = a
+                               bytes, 16-byte aligned, not overlapping q/k/v/out/lse; NULL = a
                                library-owned per-device buffer (allocated or grown with
                                cudaMalloc on first need; shared by every call on that device, so
                                calls that may overlap on different streams should pass their own) */

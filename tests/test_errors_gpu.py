@@ -71,3 +71,25 @@ def test_pipeline_wait_timeout_is_reported_and_context_stays_usable():
     vdx.sync_check()
     ref_o, _ = O.rope3d_attention(q, k, v, (1, 2, 64))
     assert np.abs(o2.double().cpu().numpy() - ref_o).max() <= 2e-2
+
+
+def test_caller_workspace_next_to_an_input_is_accepted_and_an_overlap_rejected():
+    # Split precision: the workspace is twice the size of q, so a check that sized q like the
+    # workspace would flag a workspace that merely starts where q ends.
+    w = dataclasses.replace(configs.LONG_STRESS, B=1, H=2, T=1, Hg=4, Wg=64, seed=33)
+    q, k, v = (t.cuda() for t in synth.make_qkv(w))
+    grid = (w.T, w.Hg, w.Wg)
+    need = vdx.workspace_bytes(w.B, w.H, grid, w.d, vdx.QK_SPLIT)
+    buf = torch.empty(q.numel() + need // 2, dtype=torch.bfloat16, device="cuda")
+    qa = buf[:q.numel()].view(q.shape)
+    qa.copy_(q)
+    out, lse = vdx.rope3d_attn(qa, k, v, grid, w.sections, w.theta, workspace=buf[q.numel():],
+                               qk_precision=vdx.QK_SPLIT)
+    ref_o, ref_l = vdx.rope3d_attn(q, k, v, grid, w.sections, w.theta, qk_precision=vdx.QK_SPLIT)
+    vdx.sync_check()
+    assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
+    with pytest.raises(vdx.VdxError) as ei:
+        vdx.rope3d_attn(qa, k, v, grid, w.sections, w.theta, workspace=buf[q.numel() // 2:],
+                        qk_precision=vdx.QK_SPLIT)
+    assert ei.value.status == 1 and "overlaps" in str(ei.value)
+    vdx.sync_check()

@@ -251,10 +251,13 @@ static vdx_status attn_bf16(const void* q, const void* k, const void* v, void* o
                     opt->workspace_bytes, need);
       if (reinterpret_cast<uintptr_t>(opt->workspace) & 15)
         return fail(VDX_ERR_ALIGN, "workspace is not 16-byte aligned");
-      const size_t bytes = need;
-      if (overlaps(opt->workspace, bytes, q, bytes) || overlaps(opt->workspace, bytes, k, bytes) ||
-          overlaps(opt->workspace, bytes, v, bytes) || overlaps(opt->workspace, bytes, out, bytes))
-        return fail(VDX_ERR_ARG, "workspace overlaps q, k, v or out");
+      // q, k, v and out each span B*N*H*d bf16 values; the workspace spans `need` bytes
+      // (twice a tensor in the split mode).
+      const size_t tb = static_cast<size_t>(p.B) * p.N * p.H * p.d * 2;
+      if (overlaps(opt->workspace, need, q, tb) || overlaps(opt->workspace, need, k, tb) ||
+          overlaps(opt->workspace, need, v, tb) || overlaps(opt->workspace, need, out, tb) ||
+          (lse && overlaps(opt->workspace, need, lse, static_cast<size_t>(p.B) * p.H * p.N * 4)))
+        return fail(VDX_ERR_ARG, "workspace overlaps q, k, v, out or lse");
       ws = opt->workspace;
     } else if ((s = get_workspace(need, &ws)) != VDX_OK) {
       return s;
