@@ -420,7 +420,7 @@ def run_ours(args, w):
                          "frac": tflops_rank / peak, "traffic": traffic,
                          "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)",
                          "frac_of_sustained": (tflops_rank / peak_sus) if peak_sus else None,
-                         "kernel": "attn_fwd_sm103 (+ rope3d_k_prepass)" if args.k_rope == "prepass"
+                         "kernel": "attn_fwd_sm103 (+ rope3d_qk_prepass)" if args.k_rope == "prepass"
                          else "attn_fwd_sm103 (fused K rotation)"},
             "cpu_baseline": cpu,
             "clocks": clocks,

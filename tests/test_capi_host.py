@@ -70,8 +70,9 @@ def test_rejects_bad_arguments_without_cuda(L, kw, status, msg):
 
 
 def test_workspace_bytes(L):
-    assert L.vdx_rope3d_workspace_bytes(2, 40, 21, 45, 80, 128, 0) == 2 * 75600 * 40 * 128 * 2
-    assert L.vdx_rope3d_workspace_bytes(2, 40, 21, 45, 80, 128, 1) == 2 * 75600 * 40 * 128 * 4
+    # rotated K and rotated Q (fp16 each), doubled again for the hi + lo split
+    assert L.vdx_rope3d_workspace_bytes(2, 40, 21, 45, 80, 128, 0) == 2 * 75600 * 40 * 128 * 2 * 2
+    assert L.vdx_rope3d_workspace_bytes(2, 40, 21, 45, 80, 128, 1) == 2 * 75600 * 40 * 128 * 4 * 2
     assert L.vdx_rope3d_workspace_bytes(0, 40, 21, 45, 80, 128, 0) == 0
 
 

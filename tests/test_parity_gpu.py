@@ -86,7 +86,7 @@ def test_bf16_caller_workspace_matches_library_workspace():
     w = dataclasses.replace(configs.WAN13B_480P, B=2, H=2, T=2, Hg=7, Wg=19, seed=25)
     q, k, v = (t.cuda() for t in synth.make_qkv(w))
     nbytes = vdx.workspace_bytes(w.B, w.H, (w.T, w.Hg, w.Wg))
-    assert nbytes == q.numel() * 2
+    assert nbytes == 2 * q.numel() * 2          # rotated K and rotated Q, fp16 each
     ws = torch.empty(nbytes // 2 + 64, dtype=torch.float16, device="cuda")
     o1, l1 = _run(w, q, k, v, workspace=ws)
     o2, l2 = _run(w, q, k, v)
@@ -99,6 +99,15 @@ def test_bf16_caller_workspace_matches_library_workspace():
     with pytest.raises(vdx.VdxError) as ei:
         vdx.rope3d_attn(q, k, v, (w.T, w.Hg, w.Wg), workspace=ws[:100])
     assert ei.value.status == 1
+    # A query subset rotates its gathered rows itself: the rotated-K half of the workspace is
+    # enough, and every row then matches the dense call.
+    idx = torch.arange(w.N, dtype=torch.int32, device="cuda")
+    o4, l4 = torch.zeros_like(o1), torch.zeros_like(l1)
+    vdx.rope3d_attn_subset(q, k, v, (w.T, w.Hg, w.Wg), idx, o4, l4, w.sections, w.theta,
+                           workspace=ws[:q.numel()])
+    vdx.sync_check()
+    assert (o4.float() - o1.float()).abs().max().item() <= 2e-3
+    assert (l4 - l1).abs().max().item() <= 1e-4
 
 
 def test_bf16_custom_sections_theta_scale():

@@ -123,6 +123,7 @@ struct Params {
   long long q_index_b_stride;  // entries between consecutive batches' lists (0: shared list)
   const __nv_bfloat16* q;      // q itself, for the gather
   int withhold_kv;             // testing only: the producer issues no K/V copy (waits expire)
+  int q_prerot;                // Q arrives rotated and scaled (fp16, from the prepass) via TMA
   const uint32_t* kv_mask;     // nullptr: every key tile
   int mask_words;              // words per query block
   long long mask_bh_stride;    // words between consecutive (b, h) masks (0: one shared mask)
@@ -387,7 +388,7 @@ template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_klo,
-               const Params p) {
+               const __grid_constant__ CUtensorMap tm_qlo, const Params p) {
   using Lo = Layout<kMode>;
   constexpr bool kFusedK = Lo::kFusedK;
   constexpr bool kSplit = Lo::kSplit;
@@ -463,12 +464,19 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       if (kSplit) tma_prefetch_desc(&tm_klo);
+      const bool q_lo = kSplit && p.q_prerot;               // Q remainders come from the prepass too
+      if (q_lo) tma_prefetch_desc(&tm_qlo);
       for (int i = 0; i < kQTiles && q_idx == nullptr; ++i) {   // a query subset is gathered by WG2
         const uint32_t bar = smem_addr(&ctl->q_full[i]);
-        mbar_arrive_expect_tx(bar, kTileBytes);
+        mbar_arrive_expect_tx(bar, q_lo ? 2 * kTileBytes : kTileBytes);
         const uint32_t dst = sQ + i * kTileBytes;
         tma_load_4d(dst, &tm_q, bar, 0, h, q0 + i * kBM, b);
         tma_load_4d(dst + kHalfBytes, &tm_q, bar, 64, h, q0 + i * kBM, b);
+        if (q_lo) {
+          const uint32_t dlo = smem_addr(smem + Lo::kOffQlo) + i * kTileBytes;
+          tma_load_4d(dlo, &tm_qlo, bar, 0, h, q0 + i * kBM, b);
+          tma_load_4d(dlo + kHalfBytes, &tm_qlo, bar, 64, h, q0 + i * kBM, b);
+        }
       }
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < nkv && !p.withhold_kv; ++j) {
@@ -516,8 +524,11 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       constexpr uint32_t kIdQK = idesc_f16kind_f32acc(kBM, kBN, 0, 0);   // fp16 Q', K'
       constexpr uint32_t kIdPV = idesc_f16kind_f32acc(kBM, kD, 1, 1);   // bf16 P, V (MN-major)
       const uint32_t tS0 = tmem + 0, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
-      bool ok = mbar_wait(smem_addr(&ctl->q_ready[0]), 0, abort_flag, kSiteQReady) &&
-                mbar_wait(smem_addr(&ctl->q_ready[1]), 0, abort_flag, kSiteQReady);
+      // Q tiles are ready when their copies land (pre-rotated by the prepass) or once WG2 has
+      // rotated them in shared memory.
+      const uint64_t* qbar = p.q_prerot ? ctl->q_full : ctl->q_ready;
+      bool ok = mbar_wait(smem_addr(&qbar[0]), 0, abort_flag, kSiteQReady) &&
+                mbar_wait(smem_addr(&qbar[1]), 0, abort_flag, kSiteQReady);
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after_sync();
       // K tile j is ready: waited for at the top of step j with a one-stage ring (split mode:
@@ -588,7 +599,7 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const RopeLane L = make_rope_lane(t & 15, p.half_t, p.half_h, p.half_w, p.off_h, p.off_w);
     bool ok = true;
     float amax = 0.f;
-    for (int i = 0; i < kQTiles && ok; ++i) {
+    for (int i = 0; i < kQTiles && ok && !p.q_prerot; ++i) {
       if (q_idx) {
         amax = fmaxf(amax, rope_gather_tile<kSplit>(p, L, t, smem + Lo::kOffQ + i * kTileBytes, q_idx,
                                                     q0 + i * kBM, b, h, tab, p.scale_log2,
@@ -730,14 +741,19 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   }
 }
 
-// K prepass: rotate every token of K once (bf16 in, fp16 out, same [B, N, H, d] layout; with
-// kLo the fp16 remainders follow as a second [B, N, H, d] tensor).
+// Q/K prepass: rotate every token of K (blockIdx.y = 0) and of Q (blockIdx.y = 1, multiplied
+// by scale*log2(e)) once: bf16 in, fp16 out, same [B, N, H, d] layout; with kLo the fp16
+// remainders follow each tensor as a second [B, N, H, d] tensor.
 // One thread per 16-byte chunk; the grid stride is a multiple of 16 chunks, so each thread
 // keeps one chunk column (and its four rotary pairs) throughout.
 template <bool kLo>
 __global__ void __launch_bounds__(256)
-rope3d_k_prepass(const uint4* __restrict__ k, uint4* __restrict__ kr, const Params p,
-                 uint32_t n_chunks) {
+rope3d_qk_prepass(const uint4* __restrict__ k, uint4* __restrict__ kr, const uint4* __restrict__ q,
+                  uint4* __restrict__ qr, const Params p, uint32_t n_chunks) {
+  const bool is_q = blockIdx.y == 1;
+  const uint4* __restrict__ src = is_q ? q : k;
+  uint4* __restrict__ dst = is_q ? qr : kr;
+  const float qs = is_q ? p.scale_log2 : 1.f;
   const uint32_t stride = gridDim.x * blockDim.x;
   uint32_t c = blockIdx.x * blockDim.x + threadIdx.x;
   const RopeLane L = make_rope_lane(static_cast<int>(c & 15), p.half_t, p.half_h, p.half_w,
@@ -750,8 +766,8 @@ rope3d_k_prepass(const uint4* __restrict__ k, uint4* __restrict__ kr, const Para
     const int rem = static_cast<int>(n) - pt * p.HgWg;
     const int ph = rem / p.Wg;
     const int pw = rem - ph * p.Wg;
-    const uint4 x = __ldg(k + c);
-    kr[c] = rotate_chunk<kLo>(x, L, pt, ph, pw, p.table, amax, kLo ? kr + n_chunks + c : nullptr);
+    const uint4 x = __ldg(src + c);
+    dst[c] = rotate_chunk<kLo>(x, L, pt, ph, pw, p.table, amax, kLo ? dst + n_chunks + c : nullptr, qs);
   }
   if (!(amax <= 65504.f)) atomicOr(&g_error_word, 2u);
 }
@@ -820,7 +836,7 @@ cudaError_t launch_attn(const Problem& pr, Params p, const CUtensorMap* maps, cu
     return cudaErrorInvalidValue;
   }
   attn_fwd_sm103<kMode><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(maps[0], maps[1], maps[2],
-                                                                              maps[3], p);
+                                                                              maps[3], maps[4], p);
   e = cudaGetLastError();
   if (e != cudaSuccess) *what = "attention kernel launch failed";
   return e;
@@ -835,24 +851,30 @@ cudaError_t read_and_clear_error_word_sm103(unsigned int* word) {
   return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
 }
 
-size_t k_prepass_workspace_bytes(const Problem& pr, bool split) {
-  return static_cast<size_t>(pr.B) * pr.N * pr.H * kD * 2 * (split ? 2 : 1);
+size_t prepass_workspace_bytes(const Problem& pr, bool split, bool with_q) {
+  return static_cast<size_t>(pr.B) * pr.N * pr.H * kD * 2 * (split ? 2 : 1) * (with_q ? 2 : 1);
 }
 
 cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, KMode mode,
-                                   void* workspace, cudaStream_t stream, const char** what) {
+                                   void* workspace, bool rotate_q_in_prepass, cudaStream_t stream,
+                                   const char** what) {
   *what = nullptr;
   Params p;
   fill_params(pr, &p);
-  CUtensorMap maps[4];
+  CUtensorMap maps[5];
   const bool fused = mode == KMode::kFused;
   const bool split = mode == KMode::kSplit;
+  const bool q_pre = !fused && rotate_q_in_prepass && pr.q_index == nullptr;
+  p.q_prerot = q_pre ? 1 : 0;
   const void* kbase = pr.k;
   const void* klo = pr.k;
+  const void* qbase = pr.q;
+  const void* qlo = pr.q;
   if (!fused) {
-    const size_t chunks = k_prepass_workspace_bytes(pr, false) / 16;
+    const size_t tb = prepass_workspace_bytes(pr, false, false);      // one fp16 tensor
+    const size_t chunks = tb / 16;
     if (chunks >= 0x40000000ull) {
-      *what = "K prepass: tensor too large";
+      *what = "Q/K prepass: tensor too large";
       return cudaErrorInvalidValue;
     }
     int sms = 148;
@@ -861,27 +883,37 @@ cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, KMod
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long want = (static_cast<long long>(chunks) + 255) / 256;
     const unsigned blocks = static_cast<unsigned>(std::min<long long>(want, static_cast<long long>(sms) * 8));
+    // Workspace: K' [K' lo] then, when Q is rotated here too, Q' [Q' lo].
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint8_t* qws = ws + tb * (split ? 2 : 1);
+    const dim3 grid(blocks, q_pre ? 2 : 1);
     if (split)
-      rope3d_k_prepass<true><<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(pr.k),
-                                                          static_cast<uint4*>(workspace), p,
-                                                          static_cast<uint32_t>(chunks));
+      rope3d_qk_prepass<true><<<grid, 256, 0, stream>>>(
+          static_cast<const uint4*>(pr.k), reinterpret_cast<uint4*>(ws), static_cast<const uint4*>(pr.q),
+          reinterpret_cast<uint4*>(qws), p, static_cast<uint32_t>(chunks));
     else
-      rope3d_k_prepass<false><<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(pr.k),
-                                                           static_cast<uint4*>(workspace), p,
-                                                           static_cast<uint32_t>(chunks));
+      rope3d_qk_prepass<false><<<grid, 256, 0, stream>>>(
+          static_cast<const uint4*>(pr.k), reinterpret_cast<uint4*>(ws), static_cast<const uint4*>(pr.q),
+          reinterpret_cast<uint4*>(qws), p, static_cast<uint32_t>(chunks));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
-      *what = "K prepass launch failed";
+      *what = "Q/K prepass launch failed";
       return e;
     }
-    kbase = workspace;
-    klo = static_cast<const uint8_t*>(workspace) + k_prepass_workspace_bytes(pr, false);
+    kbase = ws;
+    klo = ws + tb;
+    if (q_pre) {
+      qbase = qws;
+      qlo = qws + tb;
+    }
   }
   const CUtensorMapDataType kdt = fused ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  if (encode_bhnd(encode, &maps[0], pr.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr) != CUDA_SUCCESS ||
+  const CUtensorMapDataType qdt = q_pre ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (encode_bhnd(encode, &maps[0], qbase, qdt, pr) != CUDA_SUCCESS ||
       encode_bhnd(encode, &maps[1], kbase, kdt, pr) != CUDA_SUCCESS ||
       encode_bhnd(encode, &maps[2], pr.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr) != CUDA_SUCCESS ||
-      encode_bhnd(encode, &maps[3], split ? klo : kbase, kdt, pr) != CUDA_SUCCESS) {
+      encode_bhnd(encode, &maps[3], split ? klo : kbase, kdt, pr) != CUDA_SUCCESS ||
+      encode_bhnd(encode, &maps[4], split && q_pre ? qlo : qbase, qdt, pr) != CUDA_SUCCESS) {
     *what = "cuTensorMapEncodeTiled failed";
     return cudaErrorInvalidValue;
   }

@@ -242,9 +242,14 @@ static vdx_status attn_bf16(const void* q, const void* k, const void* v, void* o
     p.mask_words = (nkv + 31) / 32;
     p.mask_bh_stride = mask_per_head ? static_cast<long long>(nqb) * p.mask_words : 0;
   }
+  // Rotate Q in the prepass too when each CTA streams few key tiles (a block mask, or a short
+  // sequence): there the in-kernel rotation of the CTA's Q tiles (about 8 us) is a large share
+  // of a CTA.  Long dense sequences rotate Q in-kernel and skip the extra prepass traffic.
+  const int nkv_dense = (p.N + VDX_SPARSE_KBLOCK - 1) / VDX_SPARSE_KBLOCK;
+  const bool q_pre = !fused && p.q_index == nullptr && (block_mask != nullptr || nkv_dense < 256);
   void* ws = nullptr;
   if (!fused) {
-    const size_t need = vdx::k_prepass_workspace_bytes(p, split);
+    const size_t need = vdx::prepass_workspace_bytes(p, split, q_pre);
     if (opt && opt->workspace) {
       if (opt->workspace_bytes < need)
         return fail(VDX_ERR_ARG, "workspace of %zu bytes is smaller than the %zu needed",
@@ -267,7 +272,8 @@ static vdx_status attn_bf16(const void* q, const void* k, const void* v, void* o
   if ((s = get_encode(&enc)) != VDX_OK) return s;
   const char* what = nullptr;
   const vdx::KMode km = fused ? vdx::KMode::kFused : (split ? vdx::KMode::kSplit : vdx::KMode::kPrepass);
-  cudaError_t e = vdx::launch_attn_bf16_sm103(p, enc, km, ws, static_cast<cudaStream_t>(stream), &what);
+  cudaError_t e = vdx::launch_attn_bf16_sm103(p, enc, km, ws, q_pre, static_cast<cudaStream_t>(stream),
+                                              &what);
   if (e != cudaSuccess)
     return fail(VDX_ERR_CUDA, "%s: %s", what ? what : "launch", cudaGetErrorString(e));
   return VDX_OK;
@@ -385,7 +391,7 @@ vdx_status vdx_window_block_mask(uint32_t* mask, int T, int Hgrid, int Wgrid, in
 size_t vdx_rope3d_workspace_bytes(int B, int H, int T, int Hgrid, int Wgrid, int d,
                                   int qk_precision) {
   if (B < 1 || H < 1 || T < 1 || Hgrid < 1 || Wgrid < 1 || d < 1) return 0;
-  return static_cast<size_t>(B) * T * Hgrid * Wgrid * H * d * 2 * (qk_precision == VDX_QK_SPLIT ? 2 : 1);
+  return static_cast<size_t>(B) * T * Hgrid * Wgrid * H * d * 2 * (qk_precision == VDX_QK_SPLIT ? 2 : 1) * 2;
 }
 
 vdx_status vdx_rope3d_attn_f32(const float* q, const float* k, const float* v, float* out,

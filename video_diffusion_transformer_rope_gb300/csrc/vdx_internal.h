@@ -45,11 +45,16 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 //   kFused:   every CTA rotates its K tiles in shared memory; `workspace` is unused.
 //   kSplit:   as kPrepass, with every rotated value split into fp16 hi + lo (workspace holds
 //             both) and three QK products.
+// With rotate_q_in_prepass (kPrepass / kSplit, no query subset) the prepass also rotates Q
+// (multiplied by scale*log2(e)) into the workspace after K, and the attention kernel loads
+// it rotated; otherwise every CTA rotates its Q tiles in shared memory.
 enum class KMode { kPrepass, kFused, kSplit };
 cudaError_t launch_attn_bf16_sm103(const Problem& p, EncodeTiledFn encode, KMode mode,
-                                   void* workspace, cudaStream_t stream, const char** what);
-// Workspace bytes for kPrepass (split = false) or kSplit (split = true).
-size_t k_prepass_workspace_bytes(const Problem& p, bool split);
+                                   void* workspace, bool rotate_q_in_prepass, cudaStream_t stream,
+                                   const char** what);
+// Workspace bytes for kPrepass (split = false) or kSplit (split = true), with or without the
+// rotated Q.
+size_t prepass_workspace_bytes(const Problem& p, bool split, bool with_q);
 
 // Read the tensor-core kernel's device error word (synchronous) and reset it to 0.
 cudaError_t read_and_clear_error_word_sm103(unsigned int* word);

@@ -168,7 +168,8 @@ extern "C" vdx_status vdx_rope3d_attn_noalloc(const void* q, const void* k, cons
   p.table = table;
   p.table_entries = static_cast<int>(entries);
   const char* what = nullptr;
-  e = vdx::launch_attn_bf16_sm103(p, g_encode_fn, vdx::KMode::kPrepass, workspace, st, &what);
+  e = vdx::launch_attn_bf16_sm103(p, g_encode_fn, vdx::KMode::kPrepass, workspace,
+                                  /*rotate_q_in_prepass=*/false, st, &what);
   if (e != cudaSuccess) return fail_na(VDX_ERR_CUDA, "%s: %s", what ? what : "launch", cudaGetErrorString(e));
   return VDX_OK;
 }
