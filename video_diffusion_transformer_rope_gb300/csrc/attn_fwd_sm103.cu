@@ -388,7 +388,8 @@ template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_klo,
-               const __grid_constant__ CUtensorMap tm_qlo, const Params p) {
+               const __grid_constant__ CUtensorMap tm_qlo, const __grid_constant__ CUtensorMap tm_out,
+               const Params p) {
   using Lo = Layout<kMode>;
   constexpr bool kFusedK = Lo::kFusedK;
   constexpr bool kSplit = Lo::kSplit;
@@ -707,6 +708,9 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const bool empty = nkv == 0;
       const float inv_l = empty ? 0.f : 1.f / l_run;
       __nv_bfloat16* orow = p.out + ((static_cast<size_t>(b) * p.N + (live ? n : 0)) * p.H + h) * kD;
+      // Without a query subset the tile is staged in its Q buffer (free: every MMA that read
+      // it has completed) in the 128-byte-swizzled layout and leaves through TMA below.
+      uint8_t* stile = smem + Lo::kOffQ + qi * kTileBytes;
       uint32_t r[32];
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
@@ -720,16 +724,38 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
         for (int e2 = 0; e2 < 16; ++e2)
           pk[e2] = pack_bf16x2(__uint_as_float(r[2 * e2]) * inv_l, __uint_as_float(r[2 * e2 + 1]) * inv_l);
-        if (live) {
+        if (q_idx == nullptr) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c = ch * 4 + u;            // 16-byte chunk of the row (8 channels)
+            *reinterpret_cast<uint4*>(stile + (c >> 3) * kHalfBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4)) =
+                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          }
+        } else if (live) {
           uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
         }
       }
+      if (q_idx == nullptr) fence_proxy_async_smem();
       if (live && p.lse != nullptr)
         p.lse[(static_cast<size_t>(b) * p.H + h) * p.N + n] =
             empty ? -INFINITY : (m_run + __log2f(l_run)) * 0.69314718055994530942f;
+    }
+    if (q_idx == nullptr) {
+      // Every thread of the warpgroup gets here (also after an abort), so the barrier cannot
+      // strand anyone; one thread then stores the tile (rows past N are clipped by TMA).
+      __syncwarp();
+      named_barrier_sync(1 + qi, 128);
+      const int r0 = q0 + qi * kBM;
+      if (ok && (warp & 3) == 0 && lane == 0 && r0 < p.N) {
+        const uint32_t src = smem_addr(smem + Lo::kOffQ + qi * kTileBytes);
+        tma_store_4d(&tm_out, src, 0, h, r0, b);
+        tma_store_4d(&tm_out, src + kHalfBytes, 64, h, r0, b);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+      }
     }
   }
 
@@ -836,7 +862,7 @@ cudaError_t launch_attn(const Problem& pr, Params p, const CUtensorMap* maps, cu
     return cudaErrorInvalidValue;
   }
   attn_fwd_sm103<kMode><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(maps[0], maps[1], maps[2],
-                                                                              maps[3], maps[4], p);
+                                                                              maps[3], maps[4], maps[5], p);
   e = cudaGetLastError();
   if (e != cudaSuccess) *what = "attention kernel launch failed";
   return e;
@@ -861,7 +887,7 @@ cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, KMod
   *what = nullptr;
   Params p;
   fill_params(pr, &p);
-  CUtensorMap maps[5];
+  CUtensorMap maps[6];
   const bool fused = mode == KMode::kFused;
   const bool split = mode == KMode::kSplit;
   const bool q_pre = !fused && rotate_q_in_prepass && pr.q_index == nullptr;
@@ -913,7 +939,8 @@ cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, KMod
       encode_bhnd(encode, &maps[1], kbase, kdt, pr) != CUDA_SUCCESS ||
       encode_bhnd(encode, &maps[2], pr.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr) != CUDA_SUCCESS ||
       encode_bhnd(encode, &maps[3], split ? klo : kbase, kdt, pr) != CUDA_SUCCESS ||
-      encode_bhnd(encode, &maps[4], split && q_pre ? qlo : qbase, qdt, pr) != CUDA_SUCCESS) {
+      encode_bhnd(encode, &maps[4], split && q_pre ? qlo : qbase, qdt, pr) != CUDA_SUCCESS ||
+      encode_bhnd(encode, &maps[5], pr.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr) != CUDA_SUCCESS) {
     *what = "cuTensorMapEncodeTiled failed";
     return cudaErrorInvalidValue;
   }
