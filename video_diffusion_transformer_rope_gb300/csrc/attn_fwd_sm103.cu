@@ -113,6 +113,22 @@ struct Ctl {
   int abort_flag;
 };
 
+// Division of a non-negative 32-bit integer below 2^31 by an invariant divisor d >= 1:
+// q = (umulhi(n, m) + n) >> s with s = ceil(log2 d) and m = floor(2^32 (2^s - d) / d) + 1
+// (Granlund and Montgomery, "Division by invariant integers using multiplication", 1994).
+struct FastDiv {
+  uint32_t m, s;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t s = 0;
+  while ((1ull << s) < d) ++s;
+  const uint64_t m = ((1ull << 32) * ((1ull << s) - d)) / d + 1;
+  return FastDiv{static_cast<uint32_t>(m), s};
+}
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, FastDiv f) {
+  return (__umulhi(n, f.m) + n) >> f.s;
+}
+
 struct Params {
   int B, H, N, Hg, Wg, HgWg;
   // Optional block mask: bit kb of word kb/32 of row (b, h, query block) selects key tile kb.
@@ -124,6 +140,7 @@ struct Params {
   const __nv_bfloat16* q;      // q itself, for the gather
   int withhold_kv;             // testing only: the producer issues no K/V copy (waits expire)
   int q_prerot;                // Q arrives rotated and scaled (fp16, from the prepass) via TMA
+  FastDiv div_H, div_N, div_HgWg, div_Wg;   // the prepass's row -> token -> (t, h, w) splits
   const uint32_t* kv_mask;     // nullptr: every key tile
   int mask_words;              // words per query block
   long long mask_bh_stride;    // words between consecutive (b, h) masks (0: one shared mask)
@@ -772,30 +789,37 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 // remainders follow each tensor as a second [B, N, H, d] tensor.
 // One thread per 16-byte chunk; the grid stride is a multiple of 16 chunks, so each thread
 // keeps one chunk column (and its four rotary pairs) throughout.
-template <bool kLo>
-__global__ void __launch_bounds__(256)
-rope3d_qk_prepass(const uint4* __restrict__ k, uint4* __restrict__ kr, const uint4* __restrict__ q,
-                  uint4* __restrict__ qr, const Params p, uint32_t n_chunks) {
-  const bool is_q = blockIdx.y == 1;
-  const uint4* __restrict__ src = is_q ? q : k;
-  uint4* __restrict__ dst = is_q ? qr : kr;
-  const float qs = is_q ? p.scale_log2 : 1.f;
+template <bool kLo, bool kQ>
+__device__ __forceinline__ void rope3d_prepass_body(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                    const Params& p, uint32_t n_chunks) {
   const uint32_t stride = gridDim.x * blockDim.x;
   uint32_t c = blockIdx.x * blockDim.x + threadIdx.x;
   const RopeLane L = make_rope_lane(static_cast<int>(c & 15), p.half_t, p.half_h, p.half_w,
                                     p.off_h, p.off_w);
+  const float qs = kQ ? p.scale_log2 : 1.f;
   float amax = 0.f;
   for (; c < n_chunks; c += stride) {
     const uint32_t row = c >> 4;                       // (b*N + n)*H + h
-    const uint32_t n = (row / static_cast<uint32_t>(p.H)) % static_cast<uint32_t>(p.N);
-    const int pt = static_cast<int>(n) / p.HgWg;
+    const uint32_t bn = fast_div(row, p.div_H);         // b*N + n
+    const uint32_t n = bn - fast_div(bn, p.div_N) * static_cast<uint32_t>(p.N);
+    const int pt = static_cast<int>(fast_div(n, p.div_HgWg));
     const int rem = static_cast<int>(n) - pt * p.HgWg;
-    const int ph = rem / p.Wg;
+    const int ph = static_cast<int>(fast_div(static_cast<uint32_t>(rem), p.div_Wg));
     const int pw = rem - ph * p.Wg;
     const uint4 x = __ldg(src + c);
     dst[c] = rotate_chunk<kLo>(x, L, pt, ph, pw, p.table, amax, kLo ? dst + n_chunks + c : nullptr, qs);
   }
   if (!(amax <= 65504.f)) atomicOr(&g_error_word, 2u);
+}
+
+template <bool kLo>
+__global__ void __launch_bounds__(256)
+rope3d_qk_prepass(const uint4* __restrict__ k, uint4* __restrict__ kr, const uint4* __restrict__ q,
+                  uint4* __restrict__ qr, const Params p, uint32_t n_chunks) {
+  if (blockIdx.y == 0)
+    rope3d_prepass_body<kLo, false>(k, kr, p, n_chunks);
+  else
+    rope3d_prepass_body<kLo, true>(q, qr, p, n_chunks);
 }
 
 void fill_params(const Problem& pr, Params* p) {
@@ -818,6 +842,10 @@ void fill_params(const Problem& pr, Params* p) {
   p->kv_mask = pr.kv_mask;
   p->mask_words = pr.mask_words;
   p->mask_bh_stride = pr.mask_bh_stride;
+  p->div_H = make_fastdiv(static_cast<uint32_t>(pr.H));
+  p->div_N = make_fastdiv(static_cast<uint32_t>(pr.N));
+  p->div_HgWg = make_fastdiv(static_cast<uint32_t>(pr.Hg * pr.Wg));
+  p->div_Wg = make_fastdiv(static_cast<uint32_t>(pr.Wg));
 }
 
 CUresult encode_bhnd(EncodeTiledFn encode, CUtensorMap* map, const void* base,
