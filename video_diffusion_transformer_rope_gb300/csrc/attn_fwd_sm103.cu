@@ -1,5 +1,5 @@
 // Warp-specialised flash-attention forward with 3D RoPE for sm_103a (GB300), plus the
-// K-rotation prepass it can stream from.
+// Q/K-rotation prepass it can stream from.
 //
 // Operation: vidax: A Unified JAX Framework for Video Generative Models on Accelerator
 // Meshes, §2 "3D RoPE, 3D VAEs, and flash attention" (rotary 3D positions on Q and K, then
@@ -14,14 +14,16 @@
 //   WG0  warps 0-3   softmax + epilogue for Q tile 0 (thread = query row = TMEM lane)
 //   WG1  warps 4-7   softmax + epilogue for Q tile 1
 //   WG2  warps 8-11  RoPE: rotate the Q tiles in shared memory as they land (bf16 -> fp16,
-//                    in place), or gather + rotate a query subset straight from global
-//                    memory; in the fused-K mode also every K tile
+//                    in place) unless the prepass already did, or gather + rotate a query
+//                    subset straight from global memory; in the fused-K mode also every K tile
 //   WG3  warp 12     TMA producer: Q tiles once, then K/V tiles through the rings
 //        warp 13     tcgen05 MMA issuer (the whole warp runs the loop, one elected lane
 //                    issues) and TMEM owner; warps 14-15 idle
 //
 // K modes.  Prepass (default): a separate kernel rotates K once per token into an fp16
 // workspace and the attention kernel streams that, so no K rotation sits in the hot loop.
+// For short or block-sparse calls the prepass rotates (and scales) Q as well and the Q tiles
+// arrive ready through TMA; otherwise WG2 rotates each CTA's two Q tiles.
 // Fused: TMA brings raw bf16 K and WG2 rotates each K tile in shared memory before the MMA
 // reads it (every CTA of a head repeats this for every K tile).
 // Split (precise): as prepass, but every rotated Q/K value x is kept as two fp16 numbers,
@@ -40,6 +42,10 @@
 // Each tile's exponentials are taken against the running maximum m and kept when the row
 // sum shows every p <= 256; only otherwise (the first tile, or scores that rose) is the tile
 // maximum computed, m moved there, l and O rescaled and the row redone.
+//
+// Epilogue: each softmax warpgroup writes O/l (bf16) into its Q tile buffer, free once the
+// last MMA has completed, in the same swizzled layout, and one thread stores the tile with
+// TMA (a query subset scatters its rows with plain stores instead).
 //
 // Shared memory: Q 2x32 KB, K ring, V ring (32 KB per stage), each tile stored as two
 // 128-row x 128-byte halves in the 128-byte-swizzled layout TMA writes; then (fused mode,
