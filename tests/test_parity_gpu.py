@@ -221,3 +221,11 @@ def test_bf16_uniform_attention_closed_form(which):
     mean_v = v.double().mean(dim=1, keepdim=True)
     assert (out.double() - mean_v).abs().max().item() <= 4e-3      # bf16 P = 1 exactly; bf16 out
     assert (lse.double() - np.log(w.N)).abs().max().item() <= 1e-5
+
+
+@pytest.mark.parametrize("grid", [(1, 255, 128), (1, 1, 32641)], ids=["255_key_tiles", "256_key_tiles"])
+def test_q_rotation_paths_either_side_of_the_threshold(grid):
+    # Below 256 key tiles the prepass rotates Q; from 256 on each CTA rotates its own Q tiles.
+    w = dataclasses.replace(configs.WAN13B_480P, B=1, H=2, T=grid[0], Hg=grid[1], Wg=grid[2], seed=34)
+    mx, mean, lerr = _sampled_compare(w, rows=256)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)

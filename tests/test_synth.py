@@ -1,6 +1,8 @@
 """Seeded input recipe: shapes, determinism, element type, stress outliers (CPU only)."""
 import dataclasses
 
+import pytest
+
 import torch
 
 from video_diffusion_transformer_rope_gb300 import configs, synth
@@ -42,3 +44,12 @@ def test_sample_rows_cover_tail():
     ns = [n for _, _, n in rows]
     assert 0 in ns and w.N - 1 in ns and any(n >= (w.N // 128) * 128 for n in ns)
     assert all(0 <= b < w.B and 0 <= h < w.H and 0 <= n < w.N for b, h, n in rows)
+
+
+@pytest.mark.parametrize("grid", [(1, 255, 128), (1, 1, 128), (1, 1, 1), (3, 5, 7)])
+def test_sample_rows_stay_in_range(grid):
+    # N a multiple of 128 included: the last block starts at N - 128, not at N.
+    w = dataclasses.replace(configs.WAN13B_480P, B=1, H=2, T=grid[0], Hg=grid[1], Wg=grid[2])
+    rows = synth.sample_rows(w, 64)
+    assert all(0 <= b < w.B and 0 <= h < w.H and 0 <= n < w.N for b, h, n in rows)
+    assert any(n == ((w.N - 1) // 128) * 128 for _, _, n in rows)

@@ -58,7 +58,7 @@ def sample_rows(w, count=512, seed=None):
     g = torch.Generator(device="cpu").manual_seed(w.seed + 2000 if seed is None else seed)
     rows = set()
     bh = [(b, h) for b in range(w.B) for h in range(w.H)]
-    fixed_n = [0, w.N - 1, max(0, (w.N // 128) * 128), max(0, w.N - 2)]
+    fixed_n = [0, w.N - 1, ((w.N - 1) // 128) * 128, max(0, w.N - 2)]   # start of the last 128-row block
     for i, n in enumerate(fixed_n):
         b, h = bh[i % len(bh)]
         rows.add((b, h, n))
