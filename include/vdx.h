@@ -107,8 +107,8 @@ vdx_status vdx_rope3d_attn_ex(const void* q, const void* k, const void* v, void*
 size_t vdx_rope3d_workspace_bytes(int B, int H, int T, int Hgrid, int Wgrid, int d,
                                   int qk_precision);
 
-/* ---- Block-sparse attention (the "bit-wise block-sparse kernel" of ScalingAttention, on the
- * first thelatestinai.com page of this reference; masks here are caller-defined).  Keys are
+/* ---- Block-sparse attention (the bit-wise block-sparse kernel of the ScalingAttention abstract
+ * on the papers page 2606.17566; masks here are caller-defined).  Keys are
  * cut into tiles of VDX_SPARSE_KBLOCK tokens and queries into blocks of VDX_SPARSE_QBLOCK
  * tokens; query n attends only to the key tiles its block's mask selects (a query whose mask
  * row selects nothing gets out = 0 and lse = -inf).  Skipped tiles cost no work.
@@ -125,8 +125,9 @@ vdx_status vdx_rope3d_attn_sparse(const void* q, const void* k, const void* v, v
                                   const uint32_t* block_mask, int mask_per_head,
                                   const vdx_attn_options* opt, void* stream);
 
-/* ---- Active-query subset (after the step-skipping scheme on the first thelatestinai.com page
- * of this reference, where only active query tokens are recomputed against the full K/V).
+/* ---- Active-query subset (after the KV-cache synchronization of the Heterogeneous Step
+ * Allocation abstract on the papers page 2606.17566: only active query tokens are recomputed,
+ * against the full K/V).
  * Query rows are the tokens q_index[i], i < Nq (device int32; one list shared by every batch
  * entry when index_per_batch = 0, else [B][Nq]); each is rotated at its own grid position,
  * attends to all N keys, and its result is written to out[b, q_index[i], h, :] and

@@ -1,8 +1,8 @@
 """Build libvdx.so in-tree with nvcc for sm_103a (GB300).
 
 Each .cu file is compiled to an object in parallel, then linked into one shared library with
-the CUDA runtime linked statically (so the library loads on machines without a GPU driver;
-the driver is reached only when a call is made).  Run `python -m
+the CUDA runtime linked statically (so the library loads on machines without the NVIDIA driver;
+libcuda is reached only when a call is made).  Run `python -m
 video_diffusion_transformer_rope_gb300._build` or call build().
 """
 import concurrent.futures as cf
