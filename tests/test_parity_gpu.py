@@ -147,6 +147,22 @@ def test_bf16_late_logit_jump():
     assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
 
 
+@pytest.mark.parametrize("first", [458, 392], ids=["second_half", "first_half"])
+def test_bf16_logit_jump_within_a_tile(first):
+    # Ten keys of the last tile (tokens 384..511) scaled x25: at 458 they sit in its second
+    # half (keys 64..127 of the tile), at 392 in its first half, so both repair routes of the
+    # softmax run (the first half already stored, or nothing stored yet).  A jump that large
+    # needs the split operands to hold the lse tolerance (see the late-jump test above).
+    w = dataclasses.replace(configs.WAN13B_480P, B=1, H=2, T=4, Hg=8, Wg=16, seed=35, qk="split")
+    q, k, v = synth.make_qkv(w)
+    k = k.float()
+    k[:, first:first + 10] *= 25.0
+    k = k.to(torch.bfloat16)
+    dev = tuple(t.cuda() for t in (q, k, v))
+    mx, mean, lerr = _full_compare(w, dev)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
+
+
 def test_bf16_deterministic_and_guard_bands():
     w = dataclasses.replace(configs.WAN13B_480P, B=1, H=2, T=2, Hg=10, Wg=13, seed=24)
     q, k, v = (t.cuda() for t in synth.make_qkv(w))
