@@ -98,12 +98,10 @@ vdx_status vdx_rope3d_attn_ex(const void* q, const void* k, const void* v, void*
                               int sec_t, int sec_h, int sec_w, double theta, float scale,
                               const vdx_attn_options* opt, void* stream);
 
-/* Bytes of workspace the prepass may need for this problem: the rotated K and the rotated,
+/* Bytes of workspace the prepass needs for this problem: the rotated K and the rotated,
  * scale*log2(e)-multiplied Q as fp16 [B, N, H, d] each (2*B*N*H*d*2), twice that with
- * VDX_QK_SPLIT (hi + lo parts); 0 for invalid sizes.  Q goes through the prepass for
- * block-sparse calls and for sequences of fewer than 256 key tiles (N < 32641); otherwise,
- * and for query-subset calls, each CTA rotates its own Q rows and only the first half (the
- * rotated K) is used. */
+ * VDX_QK_SPLIT (hi + lo parts); 0 for invalid sizes.  A query-subset call rotates its gathered
+ * rows itself and uses only the first half (the rotated K). */
 size_t vdx_rope3d_workspace_bytes(int B, int H, int T, int Hgrid, int Wgrid, int d,
                                   int qk_precision);
 

@@ -239,9 +239,12 @@ def test_bf16_uniform_attention_closed_form(which):
     assert (lse.double() - np.log(w.N)).abs().max().item() <= 1e-5
 
 
-@pytest.mark.parametrize("grid", [(1, 255, 128), (1, 1, 32641)], ids=["255_key_tiles", "256_key_tiles"])
-def test_q_rotation_paths_either_side_of_the_threshold(grid):
-    # Below 256 key tiles the prepass rotates Q; from 256 on each CTA rotates its own Q tiles.
+@pytest.mark.parametrize("grid", [(1, 255, 128), (1, 1, 32641)], ids=["N_multiple_of_128", "N_one_past"])
+@pytest.mark.parametrize("k_rope", ["prepass", "fused"])
+def test_long_rows_with_and_without_a_ragged_tile(grid, k_rope):
+    # N = 255*128 (no ragged key tile) and N = 256*128 + 1 (a last tile of one key); the prepass
+    # mode rotates Q in the prepass, the fused mode in every CTA.
     w = dataclasses.replace(configs.WAN13B_480P, B=1, H=2, T=grid[0], Hg=grid[1], Wg=grid[2], seed=34)
-    mx, mean, lerr = _sampled_compare(w, rows=256)
+    kw = {} if k_rope == "prepass" else {"k_rope": vdx.K_ROPE_FUSED}
+    mx, mean, lerr = _sampled_compare(w, rows=256, **kw)
     assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)

@@ -22,8 +22,9 @@
 //
 // K modes.  Prepass (default): a separate kernel rotates K once per token into an fp16
 // workspace and the attention kernel streams that, so no K rotation sits in the hot loop.
-// For short or block-sparse calls the prepass rotates (and scales) Q as well and the Q tiles
-// arrive ready through TMA; otherwise WG2 rotates each CTA's two Q tiles.
+// The prepass rotates (and scales) Q as well and the Q tiles arrive ready through TMA; only a
+// query subset (gathered rows), the fused-K mode and the no-allocation entry have WG2 rotate
+// each CTA's Q tiles.
 // Fused: TMA brings raw bf16 K and WG2 rotates each K tile in shared memory before the MMA
 // reads it (every CTA of a head repeats this for every K tile).
 // Split (precise): as prepass, but every rotated Q/K value x is kept as two fp16 numbers,

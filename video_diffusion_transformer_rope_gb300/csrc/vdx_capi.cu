@@ -242,11 +242,10 @@ static vdx_status attn_bf16(const void* q, const void* k, const void* v, void* o
     p.mask_words = (nkv + 31) / 32;
     p.mask_bh_stride = mask_per_head ? static_cast<long long>(nqb) * p.mask_words : 0;
   }
-  // Rotate Q in the prepass too when each CTA streams few key tiles (a block mask, or a short
-  // sequence): there the in-kernel rotation of the CTA's Q tiles (about 8 us) is a large share
-  // of a CTA.  Long dense sequences rotate Q in-kernel and skip the extra prepass traffic.
-  const int nkv_dense = (p.N + VDX_SPARSE_KBLOCK - 1) / VDX_SPARSE_KBLOCK;
-  const bool q_pre = !fused && p.q_index == nullptr && (block_mask != nullptr || nkv_dense < 256);
+  // The prepass rotates Q as well (one bandwidth-bound pass at copy speed) instead of every CTA
+  // rotating its two Q tiles in shared memory (about 8 us per CTA, latency-bound).  A query
+  // subset gathers and rotates its rows in the kernel.
+  const bool q_pre = !fused && p.q_index == nullptr;
   void* ws = nullptr;
   if (!fused) {
     const size_t need = vdx::prepass_workspace_bytes(p, split, q_pre);
