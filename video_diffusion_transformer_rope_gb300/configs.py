@@ -5,7 +5,7 @@ Framework for Video Generative Models on Accelerator Meshes", §4 "Experimental 
 App. B: batch 1 with classifier-free guidance, i.e. an internal batch of 2; 480p and native
 720p Wan2.1 1.3B / 14B).  Token index n = t*Hg*Wg + h*Wg + w.
 """
-from dataclasses import dataclass, field
+from dataclasses import dataclass
 
 
 @dataclass(frozen=True)
