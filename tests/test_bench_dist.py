@@ -35,7 +35,7 @@ def _rank(rank, ws, port, results):
 def test_two_gloo_replicas_aggregate():
     ws = 2
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     results = mgr.dict()
     mp.spawn(_rank, args=(ws, port, results), nprocs=ws, join=True)
     assert results[0][0] == results[1][0] == 125.0

@@ -19,7 +19,8 @@ def L():
 
 
 def _declared():
-    hdr = open(os.path.join(ROOT, "include", "vdx.h")).read()
+    with open(os.path.join(ROOT, "include", "vdx.h")) as f:
+        hdr = f.read()
     hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
     return set(re.findall(r"^\s*(?:vdx_status|const char\s*\*|void|int|size_t)\s+(vdx_\w+)\s*\(", hdr, re.M))
 

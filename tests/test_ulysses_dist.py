@@ -50,7 +50,7 @@ def _rank(rank, ws, port, grid, H, results):
 @pytest.mark.parametrize("ws,grid,H", [(2, (2, 4, 6), 4), (4, (2, 4, 6), 8)])
 def test_ulysses_matches_oracle(ws, grid, H):
     port = _free_port()
-    results = mp.Manager().dict()
+    results = mp.get_context("spawn").Manager().dict()
     mp.spawn(_rank, args=(ws, port, grid, H, results), nprocs=ws, join=True)
     N = grid[0] * grid[1] * grid[2]
     for r in range(ws):
