@@ -52,7 +52,11 @@ def _call(L, fn="vdx_rope3d_attn", q=FAKE, k=FAKE + (1 << 32), v=FAKE + (2 << 32
     (dict(q=0), _binding.VDX_ERR_ARG, "non-NULL"),
     (dict(out=0), _binding.VDX_ERR_ARG, "non-NULL"),
     (dict(B=0), _binding.VDX_ERR_ARG, ">= 1"),
+    (dict(H=0), _binding.VDX_ERR_ARG, ">= 1"),
+    (dict(T=0), _binding.VDX_ERR_ARG, ">= 1"),
+    (dict(Hg=0), _binding.VDX_ERR_ARG, ">= 1"),
     (dict(Wg=-3), _binding.VDX_ERR_ARG, ">= 1"),
+    (dict(fn="vdx_rope3d_attn_f32", B=0), _binding.VDX_ERR_ARG, ">= 1"),
     (dict(st=44, sh=42, sw=41), _binding.VDX_ERR_ARG, "sections"),
     (dict(st=43, sh=43, sw=42), _binding.VDX_ERR_ARG, "sections"),
     (dict(st=40, sh=40, sw=40), _binding.VDX_ERR_ARG, "sum to d"),
