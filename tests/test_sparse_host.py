@@ -23,7 +23,8 @@ def _unpack(words, nk):
 
 @pytest.mark.parametrize("grid,window", [((3, 7, 20), (1, 2, 3)), ((4, 9, 13), (0, 0, 0)),
                                          ((2, 30, 52), (1, 4, 6)), ((5, 8, 16), (2, 1, 20)),
-                                         ((21, 45, 80), (2, 6, 10))])
+                                         ((21, 45, 80), (2, 6, 10)), ((3, 5, 7), (5, 9, 9)),
+                                         ((1, 1, 1), (0, 0, 0))])
 def test_window_mask_matches_oracle(grid, window):
     N = grid[0] * grid[1] * grid[2]
     if N > 20000:
