@@ -127,7 +127,7 @@ class ClockSampler:
     def summary(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
@@ -139,6 +139,10 @@ class ClockSampler:
                     mx.append(float(parts[2]))
                 except ValueError:
                     continue
+                try:
+                    pw.append(float(parts[3]))
+                except ValueError:
+                    pw.append(float("nan"))
                 for nm, val in zip(names, parts[5:9]):
                     if val.lower() == "active":
                         reasons.add(nm)
@@ -146,8 +150,13 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        watts = [w for w in pw if w == w]
+        out = {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "samples": len(sm),
+               "reasons": sorted(reasons)}
+        if watts:
+            out["power_w_median"] = statistics.median(watts)
+            out["power_w_max"] = max(watts)
+        return out
 
 
 def _dist():
