@@ -183,20 +183,37 @@ def job_tflops(work_per_rank, ms_per_step_max, ws):
     return ws * work_per_rank / (ms_per_step_max * 1e-3) / 1e12
 
 
-def _cpu_oracle_sample(w, q, k, v, heads, rows_per_head, seed=0):
-    """Time the oracle (as it stands) on rows_per_head query rows of `heads` (b, h) pairs.
-    Inputs are already on the host.  Returns (seconds, rows)."""
+# One oracle sample: ORACLE_HEADS (b, h) pairs x ORACLE_ROWS query rows each.  The CPU
+# baseline leg of the GPU run and the reference arm time the very same samples, so their
+# TFLOP/s agree up to noise (the oracle rotates a head's K once per sample, so the per-row
+# cost depends on the rows per head).
+ORACLE_HEADS, ORACLE_ROWS = 2, 512
+
+
+def _cpu_oracle_sample(w, q, k, v, seed=0):
+    """Time the oracle (as it stands) on one sample of the workload, inputs already on the
+    host.  Returns (seconds, rows)."""
     import numpy as np
     import oracle.fp64 as O
     rng = np.random.default_rng(seed)
     rows = []
-    for i in range(heads):
-        b, h = (i % w.B), (i * 7) % w.H
-        for n in rng.choice(w.N, rows_per_head, replace=False):
+    for i in range(ORACLE_HEADS):
+        b, h = ((seed + i) % w.B), ((seed + i) * 7) % w.H
+        for n in rng.choice(w.N, ORACLE_ROWS, replace=False):
             rows.append((b, h, int(n)))
     t0 = time.perf_counter()
     O.rope3d_attention_rows(q, k, v, (w.T, w.Hg, w.Wg), rows, w.sections, w.theta)
     return time.perf_counter() - t0, len(rows)
+
+
+def _oracle_tflops(w, seconds, rows):
+    return 4.0 * w.N * w.d * rows / seconds / 1e12
+
+
+def _sample_text(w, samples, seconds):
+    return (f"{samples} sample(s) of {ORACLE_HEADS * ORACLE_ROWS} query rows ({ORACLE_HEADS} heads x "
+            f"{ORACLE_ROWS}) of the {w.name} workload, fp64 NumPy oracle, {seconds:.1f} s in all; "
+            f"TFLOP/s = 4*N*d per row / time")
 
 
 def run_reference(args, w):
@@ -208,33 +225,43 @@ def run_reference(args, w):
         q, k, v = (t.cpu() for t in synth.make_qkv(w, device="cuda"))
     else:
         q, k, v = synth.make_qkv(w, device="cpu")
-    flops_per_row = 4.0 * w.N * w.d
-    heads, rph = 2, 512
-    for _ in range(args.warmup):
-        _cpu_oracle_sample(w, q, k, v, heads, rph)
-    times = []
-    rows = 0
+    for i in range(args.warmup):
+        _cpu_oracle_sample(w, q, k, v, seed=1000 + i)
+    total_s, total_rows = 0.0, 0
     for s in range(args.steps):
-        dt, rows = _cpu_oracle_sample(w, q, k, v, heads, rph, seed=s)
-        times.append(dt)
-    per_step = sum(times) / len(times)
-    tflops = flops_per_row * rows / per_step / 1e12
-    full_ms = w.flops / (tflops * 1e12) * 1e3
+        dt, rows = _cpu_oracle_sample(w, q, k, v, seed=s)
+        total_s += dt
+        total_rows += rows
+    tflops = _oracle_tflops(w, total_s, total_rows)
+    per_step_ms = total_s / args.steps * 1e3
     cores = os.cpu_count()
     line = {
         "impl": "reference", "metric": metric_for(w), "value": tflops, "unit": "TFLOP/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": full_ms,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step_ms,
+        "ms_per_step_extrapolated": w.flops / (tflops * 1e12) * 1e3,
+        "step": f"one sample of {ORACLE_HEADS * ORACLE_ROWS} query rows (measured); "
+                "ms_per_step_extrapolated = the time of a full call at the same rate",
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1), bf16-rounded)",
         "config": _config(w),
         "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{rows} query rows ({heads} heads x {rph}) of the full workload "
-                                   f"per step, fp64 NumPy, extrapolated to a full call "
-                                   f"({per_step:.2f} s per sample)"},
+                         "sample": _sample_text(w, args.steps, total_s)},
         "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def cpu_baseline(w, q, k, v, min_seconds=8.0, max_samples=16):
+    """The same oracle samples as the reference arm, timed until min_seconds have passed."""
+    total_s, total_rows, n = 0.0, 0, 0
+    while n < max_samples and (total_s < min_seconds or n == 0):
+        dt, rows = _cpu_oracle_sample(w, q, k, v, seed=n)
+        total_s += dt
+        total_rows += rows
+        n += 1
+    return {"value": _oracle_tflops(w, total_s, total_rows), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle", "sample": _sample_text(w, n, total_s)}
 
 
 def _config(w, k_rope="prepass"):
@@ -401,13 +428,7 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.window and not args.subset:
-        hq64, hk64, hv64 = hq, hk, hv
-        heads, rph = 16, 256
-        dt, rows = _cpu_oracle_sample(w, hq64, hk64, hv64, heads, rph)
-        cpu_tf = 4.0 * w.N * w.d * rows / dt / 1e12
-        cpu = {"value": cpu_tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{rows} query rows ({heads} heads x {rph}) of this workload, fp64 NumPy "
-                         f"oracle, {dt:.1f} s, extrapolated to TFLOP/s"}
+        cpu = cpu_baseline(w, hq, hk, hv)
 
     if rank == 0:
         line = {

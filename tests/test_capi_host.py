@@ -74,6 +74,20 @@ def test_rejects_bad_arguments_without_cuda(L, kw, status, msg):
     assert msg in L.vdx_last_error().decode()
 
 
+@pytest.mark.parametrize("kw,status,msg", [
+    (dict(out=FAKE + 64), _binding.VDX_ERR_ARG, "out overlaps"),
+    (dict(lse=FAKE + (1 << 32) + 4096), _binding.VDX_ERR_ARG, "lse overlaps"),   # inside k
+    (dict(lse=FAKE + (3 << 32) + 16), _binding.VDX_ERR_ARG, "lse overlaps"),     # inside out
+    (dict(lse=FAKE - 16), _binding.VDX_ERR_ARG, "lse overlaps"),                 # its tail runs into q
+    (dict(lse=FAKE + (4 << 32) + 4), _binding.VDX_ERR_ALIGN, "aligned"),
+    (dict(d=64), _binding.VDX_ERR_UNSUPPORTED, "128"),
+])
+def test_noalloc_rejects_aliasing_without_cuda(L, kw, status, msg):
+    # the no-allocation entry checks its arguments like the ordinary one, before any CUDA call
+    assert _call(L, fn="vdx_rope3d_attn_noalloc", **kw) == status
+    assert msg in L.vdx_last_error().decode()
+
+
 def test_workspace_bytes(L):
     # rotated K and rotated Q (fp16 each), doubled again for the hi + lo split
     assert L.vdx_rope3d_workspace_bytes(2, 40, 21, 45, 80, 128, 0) == 2 * 75600 * 40 * 128 * 2 * 2

@@ -90,8 +90,9 @@ def test_out_of_range_index_is_skipped_and_reported():
     assert torch.all(out[0, keep] == 3.0)
 
 
-def test_ulysses_single_rank_on_gpu_equals_direct_call():
-    # One NCCL rank on this GPU: the exchanges are identities and the library does the work.
+def test_ulysses_single_rank_nccl_on_gpu_matches_oracle():
+    # One NCCL rank on this GPU: the exchanges are identities and the library does the work;
+    # the result is checked against the oracle and equals the direct library call bit for bit.
     import os
     import socket
     import torch.distributed as dist
@@ -105,8 +106,13 @@ def test_ulysses_single_rank_on_gpu_equals_direct_call():
     try:
         w = dataclasses.replace(configs.WAN13B_480P, B=2, H=4, T=2, Hg=8, Wg=20, seed=65)
         q, k, v = (t.cuda() for t in synth.make_qkv(w))
-        o1, l1 = ulysses_rope3d_attn(q, k, v, (w.T, w.Hg, w.Wg))
-        o2, l2 = vdx.rope3d_attn(q, k, v, (w.T, w.Hg, w.Wg))
+        o1, l1 = ulysses_rope3d_attn(q, k, v, (w.T, w.Hg, w.Wg), w.sections, w.theta)
+        vdx.sync_check()
+        ref_o, ref_l = O.rope3d_attention(q, k, v, (w.T, w.Hg, w.Wg), w.sections, w.theta)
+        err = np.abs(o1.double().cpu().numpy() - ref_o)
+        assert err.max() <= BF16_MAX and err.mean() <= BF16_MEAN, (err.max(), err.mean())
+        assert np.abs(l1.double().cpu().numpy() - ref_l).max() <= LSE_TOL
+        o2, l2 = vdx.rope3d_attn(q, k, v, (w.T, w.Hg, w.Wg), w.sections, w.theta)
         vdx.sync_check()
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
     finally:

@@ -53,3 +53,23 @@ def test_sample_rows_stay_in_range(grid):
     rows = synth.sample_rows(w, 64)
     assert all(0 <= b < w.B and 0 <= h < w.H and 0 <= n < w.N for b, h, n in rows)
     assert any(n == ((w.N - 1) // 128) * 128 for _, _, n in rows)
+
+
+def test_sample_rows_include_every_outlier_token_of_a_stress_workload():
+    # The long-clip stress workload's outlier tokens (x4 on Q and K) carry its largest logits;
+    # the sampled comparison must see every one of them as a query row.
+    w = configs.LONG_STRESS
+    _, tok = synth.outlier_indices(w)
+    assert tok.numel() == 112
+    rows = synth.sample_rows(w, 512)
+    assert len(rows) == len(set(rows)) and 512 <= len(rows) <= 512 + 112
+    by_token = {}
+    for b, h, n in rows:
+        by_token.setdefault(n, set()).add((b, h))
+    for n in tok.tolist():
+        assert n in by_token, n
+    # spread over the heads, not all on one (b, h) pair
+    outlier_bh = {bh for n in tok.tolist() for bh in by_token[n]}
+    assert len(outlier_bh) >= min(w.B * w.H, 40)
+    # an ordinary workload gets exactly `count` rows and no extra ones
+    assert len(synth.sample_rows(configs.WAN14B_720P, 512)) == 512

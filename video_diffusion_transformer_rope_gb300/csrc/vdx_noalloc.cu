@@ -146,6 +146,12 @@ extern "C" vdx_status vdx_rope3d_attn_noalloc(const void* q, const void* k, cons
       return fail_na(VDX_ERR_ALIGN, "pointer argument %d is not 16-byte aligned", i);
   if (overlap(out, bytes, q, bytes) || overlap(out, bytes, k, bytes) || overlap(out, bytes, v, bytes))
     return fail_na(VDX_ERR_ARG, "out overlaps q, k or v");
+  if (lse) {
+    const size_t lb = static_cast<size_t>(B) * H * N * sizeof(float);
+    if (overlap(lse, lb, out, bytes) || overlap(lse, lb, q, bytes) || overlap(lse, lb, k, bytes) ||
+        overlap(lse, lb, v, bytes))
+      return fail_na(VDX_ERR_ARG, "lse overlaps q, k, v or out");
+  }
 
   void* scratch = nullptr;
   vdx_status s = scratch_address(&scratch);

@@ -53,7 +53,10 @@ def sample_rows(w, count=512, seed=None):
     """Seeded (b, h, n) query rows for sampled comparison at large N.
 
     Always includes the first and last token and rows from the final (ragged) 128-row
-    block, spread over every (b, h) pair.
+    block, spread over every (b, h) pair; `count` rows in all, drawn uniformly otherwise.
+    For a stress workload every outlier token (outlier_indices) is added on top, each on one
+    (b, h) pair, taking the pairs in turn: those rows hold the largest logits, and a uniform
+    draw of a few hundred rows out of B*H*N would almost never pick one.
     """
     g = torch.Generator(device="cpu").manual_seed(w.seed + 2000 if seed is None else seed)
     rows = set()
@@ -68,4 +71,9 @@ def sample_rows(w, count=512, seed=None):
         n = int(torch.randint(w.N, (1,), generator=g))
         b, h = bh[i]
         rows.add((b, h, n))
+    if w.stress:
+        _, tok = outlier_indices(w)
+        for i, n in enumerate(sorted(int(x) for x in tok)):
+            b, h = bh[i % len(bh)]
+            rows.add((b, h, n))
     return sorted(rows)
