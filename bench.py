@@ -272,6 +272,69 @@ def _config(w, k_rope="prepass"):
             "parallelism": "replicas (one independent call per GPU)"}
 
 
+def _e2e_leg(w, q, k, v, out, lse, hq, hk, hv, call, stream, dev, barrier, max_over_ranks, work,
+             ws, steps):
+    """End to end through the public API: every step copies its inputs from pinned host memory
+    and its out + lse back, inside the timed region.  Pipelined as a serving loop would run:
+    two device buffer sets; step i+1's upload (H2D stream) and step i-1's download (D2H
+    stream) overlap step i's kernels."""
+    import torch
+    import video_diffusion_transformer_rope_gb300 as vdx
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hout = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
+    hlse = [torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True) for _ in range(2)]
+    dq, dk, dv = [q, torch.empty_like(q)], [k, torch.empty_like(k)], [v, torch.empty_like(v)]
+    dout, dlse = [out, torch.empty_like(out)], [lse, torch.empty_like(lse)]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    drained = [torch.cuda.Event() for _ in range(2)]
+    e2e_steps = max(1, steps)
+
+    def upload(i):
+        sl = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(computed[sl])          # the kernel that read this slot is done
+            dq[sl].copy_(hq, non_blocking=True)
+            dk[sl].copy_(hk, non_blocking=True)
+            dv[sl].copy_(hv, non_blocking=True)
+            in_ready[sl].record(s_in)
+
+    barrier()
+    start.record(stream)
+    s_in.wait_stream(stream)
+    s_out.wait_stream(stream)
+    upload(0)
+    for i in range(e2e_steps):
+        sl = i % 2
+        if i + 1 < e2e_steps:
+            upload(i + 1)
+        stream.wait_event(in_ready[sl])
+        if i >= 2:
+            stream.wait_event(drained[sl])             # this slot's previous result is home
+        call(dq[sl], dk[sl], dv[sl], dout[sl], dlse[sl])
+        computed[sl].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(computed[sl])
+            hout[sl].copy_(dout[sl], non_blocking=True)
+            hlse[sl].copy_(dlse[sl], non_blocking=True)
+            drained[sl].record(s_out)
+    stream.wait_stream(s_in)
+    stream.wait_stream(s_out)
+    end.record(stream)
+    barrier()
+    vdx.sync_check(stream)
+    e2e_ms = max_over_ranks(start.elapsed_time(end) / e2e_steps)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = hout[0].numel() * hout[0].element_size() + hlse[0].numel() * hlse[0].element_size()
+
+    return {"value": job_tflops(work, e2e_ms, ws), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
+            "copies": "pinned host memory, H2D and D2H streams overlapping compute "
+                      "(double-buffered device inputs and outputs)"}
+
+
 def run_ours(args, w):
     import torch
     import video_diffusion_transformer_rope_gb300 as vdx
@@ -371,58 +434,17 @@ def run_ours(args, w):
     # memory and its out + lse back, inside the timed region.  Pipelined as a serving loop
     # would run: two device buffer sets; step i+1's upload (H2D stream) and step i-1's
     # download (D2H stream) overlap step i's kernels.
-    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
-    hout = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
-    hlse = [torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True) for _ in range(2)]
-    dq, dk, dv = [q, torch.empty_like(q)], [k, torch.empty_like(k)], [v, torch.empty_like(v)]
-    dout, dlse = [out, torch.empty_like(out)], [lse, torch.empty_like(lse)]
-    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    in_ready = [torch.cuda.Event() for _ in range(2)]
-    computed = [torch.cuda.Event() for _ in range(2)]
-    drained = [torch.cuda.Event() for _ in range(2)]
-    e2e_steps = max(1, args.steps)
-
-    def upload(i):
-        sl = i % 2
-        with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(computed[sl])          # the kernel that read this slot is done
-            dq[sl].copy_(hq, non_blocking=True)
-            dk[sl].copy_(hk, non_blocking=True)
-            dv[sl].copy_(hv, non_blocking=True)
-            in_ready[sl].record(s_in)
-
-    barrier()
-    start.record(stream)
-    s_in.wait_stream(stream)
-    s_out.wait_stream(stream)
-    upload(0)
-    for i in range(e2e_steps):
-        sl = i % 2
-        if i + 1 < e2e_steps:
-            upload(i + 1)
-        stream.wait_event(in_ready[sl])
-        if i >= 2:
-            stream.wait_event(drained[sl])             # this slot's previous result is home
-        call(dq[sl], dk[sl], dv[sl], dout[sl], dlse[sl])
-        computed[sl].record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(computed[sl])
-            hout[sl].copy_(dout[sl], non_blocking=True)
-            hlse[sl].copy_(dlse[sl], non_blocking=True)
-            drained[sl].record(s_out)
-    stream.wait_stream(s_in)
-    stream.wait_stream(s_out)
-    end.record(stream)
-    barrier()
-    vdx.sync_check(stream)
-    e2e_ms = max_over_ranks(start.elapsed_time(end) / e2e_steps)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h = hout[0].numel() * hout[0].element_size() + hlse[0].numel() * hlse[0].element_size()
+    e2e = None
+    hq = hk = hv = None
+    if not args.no_e2e:
+        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        e2e = _e2e_leg(w, q, k, v, out, lse, hq, hk, hv, call, stream, dev, barrier, max_over_ranks,
+                       work, ws, args.steps)
+    elif rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        hq, hk, hv = (t.cpu() for t in (q, k, v))
 
     tflops_rank = job_tflops(work, ms, 1)
     value = job_tflops(work, ms, ws)
-    e2e_value = job_tflops(work, e2e_ms, ws)
     peak, peak_sus, peak_src = _peaks()
     traffic = _traffic_per_launch(w.name)
 
@@ -441,10 +463,7 @@ def run_ours(args, w):
                                                          "mask_density": work / w.flops}
                                                         if args.window else {}),
                            **({"active_query_fraction": float(args.subset)} if args.subset else {})),
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
-                    "copies": "pinned host memory, H2D and D2H streams overlapping compute "
-                              "(double-buffered device inputs and outputs)"},
+            "e2e": e2e,
             "gpu_launches": args.steps * (2 if args.k_rope == "prepass" else 1),
             "roofline": {"bound": "tensor", "achieved": tflops_rank, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops_rank / peak, "traffic": traffic,
@@ -478,12 +497,22 @@ def main():
     ap.add_argument("--k-rope", choices=["prepass", "fused"], default="prepass",
                     help="K rotated once by a prepass kernel (default) or per tile inside the "
                          "attention kernel")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="profiling runs only: override the workload's batch size B")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="profiling runs only: override the workload's head count H")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end leg (profiling runs: halves the device memory)")
     args = ap.parse_args()
     ws_env = int(os.environ.get("WORLD_SIZE", "1"))
     if args.gpus != ws_env:
         ap.error(f"--gpus {args.gpus} but {ws_env} process(es) were launched: run N > 1 under "
                  "torchrun (one process per GPU)")
     w = configs.BY_NAME[args.workload]
+    if args.batch or args.heads:
+        import dataclasses
+        B, H = args.batch or w.B, args.heads or w.H
+        w = dataclasses.replace(w, B=B, H=H, name=f"{w.name}_B{B}_H{H}")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)
