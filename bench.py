@@ -361,7 +361,7 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream()
 
     k_mode = {"prepass": vdx.K_ROPE_PREPASS, "fused": vdx.K_ROPE_FUSED}[args.k_rope]
-    qk = vdx.QK_SPLIT if w.qk == "split" else vdx.QK_FP16
+    qk = vdx.QK_MODES[w.qk]
     k_ws = torch.empty(vdx.workspace_bytes(w.B, w.H, grid, w.d, qk) // 2, dtype=torch.float16,
                        device=dev) if args.k_rope == "prepass" else None
 
@@ -497,6 +497,9 @@ def main():
     ap.add_argument("--k-rope", choices=["prepass", "fused"], default="prepass",
                     help="K rotated once by a prepass kernel (default) or per tile inside the "
                          "attention kernel")
+    ap.add_argument("--qk", choices=["fp16", "split"], default=None,
+                    help="QK operand precision (default: the workload's own: split for the "
+                         "long-clip stress workload, fp16 for the others)")
     ap.add_argument("--batch", type=int, default=None,
                     help="profiling runs only: override the workload's batch size B")
     ap.add_argument("--heads", type=int, default=None,
@@ -509,6 +512,9 @@ def main():
         ap.error(f"--gpus {args.gpus} but {ws_env} process(es) were launched: run N > 1 under "
                  "torchrun (one process per GPU)")
     w = configs.BY_NAME[args.workload]
+    if args.qk:
+        import dataclasses
+        w = dataclasses.replace(w, qk=args.qk)
     if args.batch or args.heads:
         import dataclasses
         B, H = args.batch or w.B, args.heads or w.H

@@ -101,11 +101,17 @@ def test_ex_rejects_bad_options(L):
                              ctypes.c_void_p(FAKE + (2 << 32)), ctypes.c_void_p(FAKE + (3 << 32)),
                              None, 1, 2, 2, 3, 4, 128, 0, 0, 0, 10000.0, 0.0, ctypes.byref(opt), None)
     assert r == _binding.VDX_ERR_ARG and "k_rope" in L.vdx_last_error().decode()
-    opt = _binding.AttnOptions(_binding.K_ROPE_FUSED, _binding.QK_SPLIT, None, 0, 0)
+    for prec in (_binding.QK_SPLIT,):
+        opt = _binding.AttnOptions(_binding.K_ROPE_FUSED, prec, None, 0, 0)
+        r = L.vdx_rope3d_attn_ex(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + (1 << 32)),
+                                 ctypes.c_void_p(FAKE + (2 << 32)), ctypes.c_void_p(FAKE + (3 << 32)),
+                                 None, 1, 2, 2, 3, 4, 128, 0, 0, 0, 10000.0, 0.0, ctypes.byref(opt), None)
+        assert r == _binding.VDX_ERR_UNSUPPORTED and "prepass" in L.vdx_last_error().decode()
+    opt = _binding.AttnOptions(_binding.K_ROPE_PREPASS, 2, None, 0, 0)
     r = L.vdx_rope3d_attn_ex(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + (1 << 32)),
                              ctypes.c_void_p(FAKE + (2 << 32)), ctypes.c_void_p(FAKE + (3 << 32)),
                              None, 1, 2, 2, 3, 4, 128, 0, 0, 0, 10000.0, 0.0, ctypes.byref(opt), None)
-    assert r == _binding.VDX_ERR_UNSUPPORTED and "prepass" in L.vdx_last_error().decode()
+    assert r == _binding.VDX_ERR_ARG and "qk_precision" in L.vdx_last_error().decode()
 
 
 def test_python_binding_rejects_mismatched_grid(L):

@@ -25,7 +25,7 @@ def _built():
 
 
 def _run(w, q, k, v, **kw):
-    kw.setdefault("qk_precision", vdx.QK_SPLIT if w.qk == "split" else vdx.QK_FP16)
+    kw.setdefault("qk_precision", vdx.QK_MODES[w.qk])
     out, lse = vdx.rope3d_attn(q, k, v, (w.T, w.Hg, w.Wg), w.sections, w.theta, **kw)
     vdx.sync_check()
     return out, lse
@@ -108,6 +108,15 @@ def test_bf16_caller_workspace_matches_library_workspace():
     vdx.sync_check()
     assert (o4.float() - o1.float()).abs().max().item() <= 2e-3
     assert (l4 - l1).abs().max().item() <= 1e-4
+
+
+@pytest.mark.parametrize("grid", [(2, 8, 16), (3, 10, 10)], ids=["N256", "N300_ragged"])
+def test_bf16_many_heads_several_waves(grid):
+    # 300 (b, h) pairs with one CTA each: about two waves of one CTA per SM, every CTA on a
+    # different head, each compared in full with the oracle.
+    w = dataclasses.replace(configs.WAN13B_480P, B=2, H=150, T=grid[0], Hg=grid[1], Wg=grid[2], seed=36)
+    mx, mean, lerr = _full_compare(w)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
 
 
 def test_bf16_custom_sections_theta_scale():

@@ -28,7 +28,7 @@ def _compare(w, mask_bool, qk="fp16", dev=None):
     q, k, v = dev if dev is not None else (t.cuda() for t in synth.make_qkv(w))
     words = torch.from_numpy(vdx.pack_block_mask(mask_bool).astype(np.int32)).cuda()
     out, lse = vdx.rope3d_attn_sparse(q, k, v, (w.T, w.Hg, w.Wg), words, w.sections, w.theta,
-                                      qk_precision=vdx.QK_SPLIT if qk == "split" else vdx.QK_FP16)
+                                      qk_precision=vdx.QK_MODES[qk])
     vdx.sync_check()
     ref_o, ref_l = O.rope3d_attention_blocksparse(q, k, v, (w.T, w.Hg, w.Wg), mask_bool,
                                                   sections=w.sections, theta=w.theta)

@@ -29,7 +29,7 @@ def _run_subset(w, idx_np, qk="fp16", seed_out=7.0):
     lse = torch.full((w.B, w.H, w.N), -5.0, device="cuda")
     idx = torch.from_numpy(np.ascontiguousarray(idx_np, dtype=np.int32)).cuda()
     vdx.rope3d_attn_subset(q, k, v, (w.T, w.Hg, w.Wg), idx, out, lse, w.sections, w.theta,
-                           qk_precision=vdx.QK_SPLIT if qk == "split" else vdx.QK_FP16)
+                           qk_precision=vdx.QK_MODES[qk])
     vdx.sync_check()
     return q, k, v, out, lse
 

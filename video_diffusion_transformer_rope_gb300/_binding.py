@@ -17,6 +17,7 @@ _p, _i, _d, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_float
 
 K_ROPE_DEFAULT, K_ROPE_PREPASS, K_ROPE_FUSED = 0, 1, 2
 QK_FP16, QK_SPLIT = 0, 1
+QK_MODES = {"fp16": QK_FP16, "split": QK_SPLIT}
 
 
 class AttnOptions(ctypes.Structure):
