@@ -63,6 +63,15 @@ typedef enum {
                                  bits): for activations whose logits reach the hundreds; about
                                  half the speed; needs the K prepass and twice its workspace  */
 
+/* Which attention kernel runs a dense bf16 call. */
+#define VDX_KERNEL_DEFAULT 0  /* VDX_KERNEL_PAIR where it applies and N >= 65536, else
+                                 VDX_KERNEL_SINGLE                                                */
+#define VDX_KERNEL_SINGLE 1   /* one CTA per 256 query rows, each streaming whole K/V tiles          */
+#define VDX_KERNEL_PAIR 2     /* clusters of two CTAs: each holds half of every K/V tile and the pair
+                                 multiplies both CTAs' 512 query rows with CTA-pair MMAs; dense
+                                 calls with the K prepass and fp16 operands only (otherwise
+                                 VDX_ERR_UNSUPPORTED)                                            */
+
 typedef struct vdx_attn_options {
   int k_rope;               /* one of VDX_K_ROPE_*                                              */
   int qk_precision;         /* one of VDX_QK_*                                                  */
@@ -76,6 +85,7 @@ typedef struct vdx_attn_options {
                                so every pipeline wait runs out (after about 1 s); the kernel then
                                stops cleanly and vdx_sync_check reports VDX_ERR_TIMEOUT (this is
                                how the failure path is exercised without faulting the GPU)    */
+  int kernel;               /* one of VDX_KERNEL_*                                              */
 } vdx_attn_options;
 
 /* bf16 path, tcgen05 tensor cores.  q, k, v, out: __nv_bfloat16 [B, N, H, d]; d must be 128.

@@ -114,6 +114,19 @@ def test_ex_rejects_bad_options(L):
     assert r == _binding.VDX_ERR_ARG and "qk_precision" in L.vdx_last_error().decode()
 
 
+@pytest.mark.parametrize("k_rope,prec,kernel,status", [
+    (_binding.K_ROPE_FUSED, _binding.QK_FP16, _binding.KERNEL_PAIR, _binding.VDX_ERR_UNSUPPORTED),
+    (_binding.K_ROPE_PREPASS, _binding.QK_SPLIT, _binding.KERNEL_PAIR, _binding.VDX_ERR_UNSUPPORTED),
+    (_binding.K_ROPE_PREPASS, _binding.QK_FP16, 9, _binding.VDX_ERR_ARG),
+])
+def test_ex_rejects_unsupported_kernel_choices(L, k_rope, prec, kernel, status):
+    opt = _binding.AttnOptions(k_rope, prec, None, 0, 0, kernel)
+    r = L.vdx_rope3d_attn_ex(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + (1 << 32)),
+                             ctypes.c_void_p(FAKE + (2 << 32)), ctypes.c_void_p(FAKE + (3 << 32)),
+                             None, 1, 2, 2, 3, 4, 128, 0, 0, 0, 10000.0, 0.0, ctypes.byref(opt), None)
+    assert r == status and "kernel" in L.vdx_last_error().decode().lower()
+
+
 def test_python_binding_rejects_mismatched_grid(L):
     import torch
     q = torch.zeros(1, 10, 1, 128)

@@ -72,6 +72,26 @@ def test_bf16_small_shapes(grid, mode):
     assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
 
 
+# CTA pairs: N = 192 and 129 (one query block, so a padding CTA completes the pair), 468, 640
+# (three blocks: padded to four), 1 (a single token), 280 (T = 7, Wg = 1).
+@pytest.mark.parametrize("grid", [(3, 8, 8), (1, 1, 129), (4, 9, 13), (5, 8, 16), (1, 1, 1), (7, 40, 1)],
+                         ids=lambda g: "x".join(map(str, g)))
+def test_bf16_cta_pair_small_shapes(grid):
+    w = dataclasses.replace(configs.WAN13B_480P, B=2, H=3, T=grid[0], Hg=grid[1], Wg=grid[2], seed=43)
+    mx, mean, lerr = _full_compare(w, kernel=vdx.KERNEL_PAIR)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
+
+
+def test_bf16_cta_pair_agrees_with_single_cta_kernel():
+    # same fp16 operands and softmax, different MMA shapes: equal to rounding
+    w = dataclasses.replace(configs.WAN13B_480P, B=2, H=5, T=3, Hg=10, Wg=30, seed=44)
+    q, k, v = (t.cuda() for t in synth.make_qkv(w))
+    o1, l1 = _run(w, q, k, v, kernel=vdx.KERNEL_SINGLE)
+    o2, l2 = _run(w, q, k, v, kernel=vdx.KERNEL_PAIR)
+    assert (o1.float() - o2.float()).abs().max().item() <= 2e-3
+    assert (l1 - l2).abs().max().item() <= 1e-4
+
+
 @pytest.mark.parametrize("grid", [(3, 8, 8), (1, 1, 129), (4, 9, 13), (7, 40, 1)],
                          ids=lambda g: "x".join(map(str, g)))
 def test_bf16_split_precision_small_shapes(grid):
@@ -244,6 +264,13 @@ def test_full_size_configs_sampled(w):
     mx, mean, lerr, stats = _sampled_compare(w)
     print(f"{w.name}: out max {mx:.3e} mean {mean:.3e} lse max {lerr:.3e} "
           + " ".join(f"{k} {v:.3e}" if isinstance(v, float) else f"{k} {v}" for k, v in stats.items()))
+    _assert_sampled(w, mx, mean, lerr, stats)
+
+
+@pytest.mark.parametrize("w", [configs.WAN13B_480P, configs.WAN14B_720P], ids=lambda w: w.name)
+def test_full_size_cta_pair_sampled(w):
+    mx, mean, lerr, stats = _sampled_compare(w, kernel=vdx.KERNEL_PAIR)
+    print(f"{w.name} (CTA pairs): out max {mx:.3e} mean {mean:.3e} lse max {lerr:.3e} {stats}")
     _assert_sampled(w, mx, mean, lerr, stats)
 
 

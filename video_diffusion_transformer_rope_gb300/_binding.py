@@ -16,6 +16,7 @@ STATUS_NAMES = {0: "VDX_OK", 1: "VDX_ERR_ARG", 2: "VDX_ERR_ALIGN", 3: "VDX_ERR_U
 _p, _i, _d, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_float
 
 K_ROPE_DEFAULT, K_ROPE_PREPASS, K_ROPE_FUSED = 0, 1, 2
+KERNEL_DEFAULT, KERNEL_SINGLE, KERNEL_PAIR = 0, 1, 2
 QK_FP16, QK_SPLIT = 0, 1
 QK_MODES = {"fp16": QK_FP16, "split": QK_SPLIT}
 
@@ -24,7 +25,7 @@ class AttnOptions(ctypes.Structure):
     """vdx_attn_options (include/vdx.h)."""
     _fields_ = [("k_rope", ctypes.c_int), ("qk_precision", ctypes.c_int),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-                ("test_withhold_kv", ctypes.c_int)]
+                ("test_withhold_kv", ctypes.c_int), ("kernel", ctypes.c_int)]
 # name -> (restype, argtypes); mirrors include/vdx.h
 SIGNATURES = {
     "vdx_rope3d_attn": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _d, _f, _p]),
@@ -84,14 +85,16 @@ def _stream_handle(stream):
 
 def rope3d_attn(q, k, v, grid, sections=(0, 0, 0), theta=10000.0, scale=0.0, out=None,
                 lse=None, return_lse=True, stream=None, k_rope=K_ROPE_DEFAULT, workspace=None,
-                qk_precision=QK_FP16):
+                qk_precision=QK_FP16, kernel=KERNEL_DEFAULT):
     """3D-RoPE attention of CUDA tensors q, k, v laid out [B, N, H, d] (bf16 with d = 128, or
     float32 with d = 64/128).  grid = (T, Hgrid, Wgrid) with N = T*Hgrid*Wgrid.
 
     bf16 only: k_rope selects how K is rotated (K_ROPE_PREPASS, the default, or K_ROPE_FUSED);
     qk_precision QK_SPLIT keeps hi + lo fp16 parts of every rotated value (three products,
     for logits in the hundreds); workspace is an optional CUDA tensor of at least
-    workspace_bytes(...) bytes for the prepass (None: the library's own per-device buffer).
+    workspace_bytes(...) bytes for the prepass (None: the library's own per-device buffer);
+    kernel selects KERNEL_SINGLE (one CTA per 256 query rows) or KERNEL_PAIR (CTA pairs sharing
+    each K/V tile; dense fp16 calls only), KERNEL_DEFAULT the library's choice.
 
     Returns (out [B, N, H, d] in the input dtype, lse [B, H, N] float32 or None).  Enqueued on
     `stream` (default: torch's current stream); call sync_check() to surface device errors.
@@ -116,12 +119,13 @@ def rope3d_attn(q, k, v, grid, sections=(0, 0, 0), theta=10000.0, scale=0.0, out
             ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr() if lse is not None else 0),
             B, H, T, Hg, Wg, d, st, sh, sw, float(theta), float(scale), _stream_handle(stream))
     if q.dtype == torch.bfloat16:
-        if k_rope == K_ROPE_DEFAULT and workspace is None and qk_precision == QK_FP16:
+        if k_rope == K_ROPE_DEFAULT and workspace is None and qk_precision == QK_FP16 and kernel == KERNEL_DEFAULT:
             _check(lib().vdx_rope3d_attn(*args))
         else:
             opt = AttnOptions(int(k_rope), int(qk_precision),
                               ctypes.c_void_p(workspace.data_ptr() if workspace is not None else 0),
-                              workspace.numel() * workspace.element_size() if workspace is not None else 0)
+                              workspace.numel() * workspace.element_size() if workspace is not None else 0,
+                              0, int(kernel))
             _check(lib().vdx_rope3d_attn_ex(*args[:-1], ctypes.byref(opt), args[-1]))
     elif q.dtype == torch.float32:
         _check(lib().vdx_rope3d_attn_f32(*args))

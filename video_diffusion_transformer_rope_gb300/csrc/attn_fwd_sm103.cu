@@ -18,7 +18,9 @@
 //                    subset straight from global memory; in the fused-K mode also every K tile
 //   WG3  warp 12     TMA producer: Q tiles once, then K/V tiles through the rings
 //        warp 13     tcgen05 MMA issuer (the whole warp runs the loop, one elected lane
-//                    issues) and TMEM owner; warps 14-15 idle
+//                    issues) and TMEM owner (in a CTA pair: rank 0 only)
+//        warp 14     rank 1 of a CTA pair: relays its landed Q/K/V halves to rank 0
+//        warp 15     idle
 //
 // K modes.  Prepass (default): a separate kernel rotates K once per token into an fp16
 // workspace and the attention kernel streams that, so no K rotation sits in the hot loop.
@@ -31,6 +33,14 @@
 // hi = fp16(x) and lo = fp16(x - hi), and S = Qhi Khi^T + Qhi Klo^T + Qlo Khi^T (about 22
 // significant bits per operand instead of 11) for inputs whose logits reach the hundreds.
 // Three QK products and one-stage K/V rings (shared memory holds Q hi+lo and K hi+lo).
+//
+// CTA pairs (long dense sequences): two CTAs of a cluster take consecutive query blocks of one
+// (b, h).  Each loads only half of every K tile (keys 0-63 or 64-127) and half of every V tile
+// (channels 0-63 or 64-127) into its own 4-stage rings, and the rank-0 CTA issues cta_group::2
+// MMAs (M = 256: both CTAs' Q tiles, N = 128 read from both CTAs' halves) that write each
+// CTA's rows into its own tensor memory; the multicast commits tell both CTAs.  Rank 1 relays
+// "my half has landed" and "my P is stored" to rank 0 with remote mbarrier arrivals.  Same
+// softmax and epilogue per CTA; half the shared-memory operand reads and L2->SM traffic.
 //
 // TMEM (512 columns x 128 lanes, fp32): S0 [0,128)  S1 [128,256)  O0 [256,384)  O1 [384,512).
 // P_i (bf16, two per column) overwrites the first 64 columns of S_i and is the A operand of
@@ -73,24 +83,30 @@ constexpr int kTileBytes = kBN * kD * 2; // 32 KB
 constexpr int kHalfBytes = kTileBytes / 2;
 constexpr int kThreads = 512;
 constexpr int kTmemCols = 512;
-constexpr int kMaxStages = 3;
+constexpr int kMaxStages = 4;
 constexpr int kMaxDynSmem = 232448;      // sm_100-family opt-in limit per CTA
 
 
-enum : int { kModePrepass = 0, kModeFused = 1, kModeSplit = 2 };
+// kModePair: the prepass mode run by a cluster of two CTAs (a CTA pair) that share every
+// K/V tile: each CTA holds half of it (keys 0-63 or 64-127 of a K tile, channels 0-63 or
+// 64-127 of a V tile) and the pair's rank-0 CTA issues cta_group::2 MMAs over both CTAs' 256
+// query rows.
+enum : int { kModePrepass = 0, kModeFused = 1, kModeSplit = 2, kModePair = 3 };
 
 template <int kMode>
 struct Layout {
   static constexpr bool kFusedK = kMode == kModeFused;
   static constexpr bool kSplit = kMode == kModeSplit;
-  static constexpr int kKStages = kMode == kModePrepass ? 3 : (kMode == kModeFused ? 2 : 1);
-  static constexpr int kVStages = kSplit ? 1 : 2;
-  static constexpr int kKStageBytes = kSplit ? 2 * kTileBytes : kTileBytes;   // hi [+ lo]
+  static constexpr bool kPair = kMode == kModePair;
+  static constexpr int kKStages = kMode == kModePrepass ? 3 : (kMode == kModeFused ? 2 : (kPair ? 4 : 1));
+  static constexpr int kVStages = kSplit ? 1 : (kPair ? 4 : 2);
+  static constexpr int kKStageBytes = kSplit ? 2 * kTileBytes : (kPair ? kTileBytes / 2 : kTileBytes);   // hi [+ lo]
+  static constexpr int kVStageBytes = kPair ? kTileBytes / 2 : kTileBytes;
   static constexpr int kOffQ = 0;                                              // Q (hi) tiles
   static constexpr int kOffQlo = kOffQ + kQTiles * kTileBytes;                 // Q lo tiles
   static constexpr int kOffK = kOffQlo + (kSplit ? kQTiles * kTileBytes : 0);
   static constexpr int kOffV = kOffK + kKStages * kKStageBytes;
-  static constexpr int kOffTab = kOffV + kVStages * kTileBytes;
+  static constexpr int kOffTab = kOffV + kVStages * kVStageBytes;
   // Registers per thread after the role split (sum over the 4 warpgroups = 512 x 128 at
   // launch); the split mode's MMA warp issues three QK chains and needs more.
   static constexpr uint32_t kRegsSoftmax = kSplit ? 160 : 184;
@@ -102,7 +118,7 @@ struct Layout {
 // Wait sites recorded in the error word when a bounded wait gives up.
 enum : int {
   kSiteQFull = 1, kSiteKFull, kSiteKReady, kSiteKEmpty, kSiteVFull, kSiteVEmpty,
-  kSiteSFull, kSitePReady, kSiteQReady, kSiteOFinal, kSiteDrain
+  kSiteSFull, kSitePReady, kSiteQReady, kSiteOFinal, kSiteDrain, kSiteRelay
 };
 
 struct Ctl {
@@ -249,6 +265,30 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
   for (int kk = 0; kk < kBN / 16; ++kk) {
     mma_ts_warp(d_tmem, p_tmem + kk * 8, smem_desc_sw128(v_smem + kk * 2048, kHalfBytes, 1024),
                 idesc, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+// Pair forms (rank-0 CTA of a pair only).  QK: A = this pair's Q tile (each CTA's 128 rows), B =
+// a K tile whose keys 0-63 sit in rank 0's stage and 64-127 in rank 1's, each stage two 8 KB
+// halves (channels 0-63, 64-127) of 64 rows x 128 bytes.  PV: A = P from each CTA's tensor
+// memory, B = V with channels 0-63 in rank 0's stage and 64-127 in rank 1's (128 keys x 128
+// bytes each, MN-major).  M = 256, N = 128 in both.
+__device__ __forceinline__ void issue_qk_pair(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
+                                              uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    const uint32_t a_off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+    const uint32_t b_off = (kk >> 2) * (kHalfBytes / 2) + (kk & 3) * 32;
+    mma_ss_pair_warp(d_tmem, smem_desc_sw128(a_smem + a_off, 16, 1024),
+                     smem_desc_sw128(b_smem + b_off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+__device__ __forceinline__ void issue_pv_pair(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                              uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk) {
+    mma_ts_pair_warp(d_tmem, p_tmem + kk * 8, smem_desc_sw128(v_smem + kk * 2048, kHalfBytes, 1024),
+                     idesc, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -417,6 +457,7 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   using Lo = Layout<kMode>;
   constexpr bool kFusedK = Lo::kFusedK;
   constexpr bool kSplit = Lo::kSplit;
+  constexpr bool kPair = Lo::kPair;
   constexpr int kKStages = Lo::kKStages;
   constexpr int kVStages = Lo::kVStages;
   extern __shared__ uint8_t smem_raw[];
@@ -447,21 +488,27 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const uint32_t sQ = smem_addr(smem + Lo::kOffQ);
   const uint32_t sK = smem_addr(smem + Lo::kOffK);
   const uint32_t sV = smem_addr(smem + Lo::kOffV);
+  // CTA pair: rank 0 (the leader) issues every MMA; its q/k/v "full" barriers also count one
+  // relayed arrival from rank 1 once rank 1's own half has landed, and its P-ready barriers
+  // one arrival from each of rank 1's softmax warps.
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0u;
+  const uint32_t full_count = (kPair && leader) ? 2u : 1u;
 
   if (tid == 0) {
     for (int i = 0; i < kQTiles; ++i) {
-      mbar_init(smem_addr(&ctl->q_full[i]), 1);
+      mbar_init(smem_addr(&ctl->q_full[i]), full_count);
       mbar_init(smem_addr(&ctl->q_ready[i]), 128);
       mbar_init(smem_addr(&ctl->s_full[i]), 1);
-      mbar_init(smem_addr(&ctl->p_ready[i]), 128);
+      mbar_init(smem_addr(&ctl->p_ready[i]), kPair ? 128 + 4 : 128);
     }
     for (int s = 0; s < kKStages; ++s) {
-      mbar_init(smem_addr(&ctl->k_full[s]), 1);
+      mbar_init(smem_addr(&ctl->k_full[s]), full_count);
       mbar_init(smem_addr(&ctl->k_ready[s]), 128);
       mbar_init(smem_addr(&ctl->k_empty[s]), 1);
     }
     for (int s = 0; s < kVStages; ++s) {
-      mbar_init(smem_addr(&ctl->v_full[s]), 1);
+      mbar_init(smem_addr(&ctl->v_full[s]), full_count);
       mbar_init(smem_addr(&ctl->v_empty[s]), 1);
     }
     mbar_init(smem_addr(&ctl->o_final), 1);
@@ -469,14 +516,20 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     fence_barrier_init();
   }
   if (warp == 13) {
-    tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_addr(&ctl->tmem_base), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
+      tmem_relinquish();
+    }
   }
   if (kFusedK && p.table_in_smem) {
     for (int i = tid; i < p.table_entries; i += kThreads) tab_s[i] = p.table[i];
   }
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();   // both CTAs' barriers exist before any remote arrive
   tc_fence_after_sync();
   const uint32_t tmem = ctl->tmem_base;
   volatile int* abort_flag = &ctl->abort_flag;
@@ -509,7 +562,16 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int ks = j % kKStages, ku = j / kKStages;
         if (ku > 0 && !mbar_wait(smem_addr(&ctl->k_empty[ks]), (ku - 1) & 1, abort_flag, kSiteKEmpty))
           break;
-        {
+        if constexpr (kPair) {
+          // this CTA's 64 keys of the tile (tm_klo holds the 64-token-box map of K here)
+          const uint32_t bar = smem_addr(&ctl->k_full[ks]);
+          mbar_arrive_expect_tx(bar, Lo::kKStageBytes);
+          const uint32_t dst = sK + ks * Lo::kKStageBytes;
+          const int row = kt * kBN + static_cast<int>(rank) * (kBN / 2);
+          tma_load_4d(dst, &tm_klo, bar, 0, h, row, b);
+          tma_load_4d(dst + kHalfBytes / 2, &tm_klo, bar, 64, h, row, b);
+          k_issued = j + 1;
+        } else {
           const uint32_t bar = smem_addr(&ctl->k_full[ks]);
           mbar_arrive_expect_tx(bar, Lo::kKStageBytes);
           const uint32_t dst = sK + ks * Lo::kKStageBytes;
@@ -526,10 +588,14 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           break;
         {
           const uint32_t bar = smem_addr(&ctl->v_full[vs]);
-          mbar_arrive_expect_tx(bar, kTileBytes);
-          const uint32_t dst = sV + vs * kTileBytes;
-          tma_load_4d(dst, &tm_v, bar, 0, h, kt * kBN, b);
-          tma_load_4d(dst + kHalfBytes, &tm_v, bar, 64, h, kt * kBN, b);
+          mbar_arrive_expect_tx(bar, Lo::kVStageBytes);
+          const uint32_t dst = sV + vs * Lo::kVStageBytes;
+          if constexpr (kPair) {
+            tma_load_4d(dst, &tm_v, bar, static_cast<int>(rank) * 64, h, kt * kBN, b);   // this CTA's 64 channels
+          } else {
+            tma_load_4d(dst, &tm_v, bar, 0, h, kt * kBN, b);
+            tma_load_4d(dst + kHalfBytes, &tm_v, bar, 64, h, kt * kBN, b);
+          }
           v_issued = j + 1;
         }
       }
@@ -543,7 +609,75 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int uses = v_issued > s ? (v_issued - 1 - s) / kVStages + 1 : 0;
         if (uses > 0) drain_wait(smem_addr(&ctl->v_full[s]), (uses - 1) & 1);
       }
-    } else if (warp == 13) {
+    } else if (kPair && warp == 13 && leader) {
+      // ---------------------------------------------------------- MMA issuer of a CTA pair:
+      // the same issue order as below with cta_group::2 MMAs over both CTAs' rows and halves;
+      // every barrier it waits on also counts arrivals from rank 1.
+      constexpr uint32_t kIdQK = idesc_f16kind_f32acc(2 * kBM, kBN, 0, 0);
+      constexpr uint32_t kIdPV = idesc_f16kind_f32acc(2 * kBM, kD, 1, 1);
+      const uint32_t tS0 = tmem + 0, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
+      bool ok = mbar_wait(smem_addr(&ctl->q_full[0]), 0, abort_flag, kSiteQReady) &&
+                mbar_wait(smem_addr(&ctl->q_full[1]), 0, abort_flag, kSiteQReady);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after_sync();
+      auto k_wait = [&](int jj) {
+        return mbar_wait(smem_addr(&ctl->k_full[jj % kKStages]), (jj / kKStages) & 1, abort_flag,
+                                 kSiteKFull);
+      };
+      if (ok && nkv > 0) ok = __all_sync(0xffffffffu, k_wait(0));
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int ks = j % kKStages;
+        tc_fence_after_sync();
+        const uint32_t kst = sK + ks * Lo::kKStageBytes;
+        issue_qk_pair(tS0, sQ, kst, kIdQK);
+        mma_commit_pair_warp(smem_addr(&ctl->s_full[0]));
+        if (j > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->p_ready[1]), (j - 1) & 1, abort_flag,
+                                                         kSitePReady));
+          if (!ok) break;
+          tc_fence_after_sync();
+          const int pvs = (j - 1) % kVStages;
+          issue_pv_pair(tO1, tS1, sV + pvs * Lo::kVStageBytes, kIdPV, j - 1 > 0);
+          mma_commit_pair_warp(smem_addr(&ctl->v_empty[pvs]));
+        }
+        issue_qk_pair(tS1, sQ + kTileBytes, kst, kIdQK);
+        mma_commit_pair_warp(smem_addr(&ctl->s_full[1]));
+        mma_commit_pair_warp(smem_addr(&ctl->k_empty[ks]));
+        const int vs = j % kVStages;
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(smem_addr(&ctl->v_full[vs]), (j / kVStages) & 1, abort_flag, kSiteVFull) &&
+                        (j + 1 >= nkv || k_wait(j + 1)) &&
+                        mbar_wait(smem_addr(&ctl->p_ready[0]), j & 1, abort_flag, kSitePReady));
+        if (!ok) break;
+        tc_fence_after_sync();
+        issue_pv_pair(tO0, tS0, sV + vs * Lo::kVStageBytes, kIdPV, j > 0);
+      }
+      if (ok && nkv > 0) {
+        const int jl = nkv - 1;
+        if (__all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->p_ready[1]), jl & 1, abort_flag, kSitePReady))) {
+          tc_fence_after_sync();
+          issue_pv_pair(tO1, tS1, sV + (jl % kVStages) * Lo::kVStageBytes, kIdPV, jl > 0);
+        }
+      }
+      mma_commit_pair_warp(smem_addr(&ctl->o_final));
+      drain_wait(smem_addr(&ctl->o_final), 0);
+    } else if (kPair && warp == 14 && lane == 0 && !leader) {
+      // ---------------------------------------------------------- relay (rank 1 of a pair):
+      // tells the leader, through one remote arrival per phase, that this CTA's Q tiles and
+      // its half of each K/V stage have landed.
+      bool ok = true;
+      for (int i = 0; ok && i < kQTiles; ++i) {
+        ok = mbar_wait(smem_addr(&ctl->q_full[i]), 0, abort_flag, kSiteRelay);
+        if (ok) mbar_arrive_remote(mapa_shared(smem_addr(&ctl->q_full[i]), 0));
+      }
+      for (int j = 0; ok && j < nkv && !p.withhold_kv; ++j) {
+        const int ks = j % kKStages, vs = j % kVStages;
+        if (!(ok = mbar_wait(smem_addr(&ctl->k_full[ks]), (j / kKStages) & 1, abort_flag, kSiteRelay))) break;
+        mbar_arrive_remote(mapa_shared(smem_addr(&ctl->k_full[ks]), 0));
+        if (!(ok = mbar_wait(smem_addr(&ctl->v_full[vs]), (j / kVStages) & 1, abort_flag, kSiteRelay))) break;
+        mbar_arrive_remote(mapa_shared(smem_addr(&ctl->v_full[vs]), 0));
+      }
+    } else if (!kPair && warp == 13) {
       // ---------------------------------------------------------- MMA issuer (whole warp runs
       // the loop so descriptor arithmetic stays warp-uniform; one elected lane issues)
       constexpr uint32_t kIdQK = idesc_f16kind_f32acc(kBM, kBN, 0, 0);   // fp16 Q', K'
@@ -716,7 +850,14 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       tmem_wait_st();
       tc_fence_before_sync();
-      mbar_arrive(smem_addr(&ctl->p_ready[qi]));
+      if (!kPair || leader) {
+        mbar_arrive(smem_addr(&ctl->p_ready[qi]));
+      } else {
+        // rank 1 of a pair: one arrival per warp on the leader's barrier, once all its lanes
+        // have stored their rows of P
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(mapa_shared(smem_addr(&ctl->p_ready[qi]), 0));
+      }
     }
     if (ok) ok = mbar_wait(smem_addr(&ctl->o_final), 0, abort_flag, kSiteOFinal);
     if (ok) {
@@ -785,9 +926,13 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();   // neither CTA leaves while the pair's MMAs may use it
   if (warp == 13) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, kTmemCols);
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -856,13 +1001,13 @@ void fill_params(const Problem& pr, Params* p) {
 }
 
 CUresult encode_bhnd(EncodeTiledFn encode, CUtensorMap* map, const void* base,
-                     CUtensorMapDataType dtype, const Problem& pr) {
+                     CUtensorMapDataType dtype, const Problem& pr, int box_tokens = kBN) {
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(pr.H),
                               static_cast<cuuint64_t>(pr.N), static_cast<cuuint64_t>(pr.B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kD) * 2,
                                  static_cast<cuuint64_t>(pr.H) * kD * 2,
                                  static_cast<cuuint64_t>(pr.N) * pr.H * kD * 2};
-  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBN), 1};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_tokens), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return encode(map, dtype, 4, const_cast<void*>(base), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -896,8 +1041,30 @@ cudaError_t launch_attn(const Problem& pr, Params p, const CUtensorMap* maps, cu
     *what = "grid too large";
     return cudaErrorInvalidValue;
   }
-  attn_fwd_sm103<kMode><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(maps[0], maps[1], maps[2],
-                                                                              maps[3], maps[4], maps[5], p);
+  if constexpr (Lo::kPair) {
+    // clusters of two CTAs (consecutive query blocks of one (b, h); n_qblk is even)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, attn_fwd_sm103<kMode>, maps[0], maps[1], maps[2], maps[3], maps[4],
+                           maps[5], p);
+    if (e != cudaSuccess) {
+      *what = "attention kernel launch (CTA pairs) failed";
+      return e;
+    }
+  } else {
+    attn_fwd_sm103<kMode><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(maps[0], maps[1], maps[2],
+                                                                                maps[3], maps[4], maps[5], p);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) *what = "attention kernel launch failed";
   return e;
@@ -925,6 +1092,14 @@ cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, KMod
   CUtensorMap maps[6];
   const bool fused = mode == KMode::kFused;
   const bool split = mode == KMode::kSplit;
+  const bool pair = mode == KMode::kPair;
+  if (pair) {
+    if (pr.q_index != nullptr || pr.kv_mask != nullptr) {
+      *what = "CTA pairs take dense calls only";
+      return cudaErrorInvalidValue;
+    }
+    p.n_qblk += p.n_qblk & 1;      // a pair's two CTAs share one (b, h)
+  }
   const bool q_pre = !fused && rotate_q_in_prepass && pr.q_index == nullptr;
   p.q_prerot = q_pre ? 1 : 0;
   const void* kbase = pr.k;
@@ -973,13 +1148,14 @@ cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, KMod
   if (encode_bhnd(encode, &maps[0], qbase, qdt, pr) != CUDA_SUCCESS ||
       encode_bhnd(encode, &maps[1], kbase, kdt, pr) != CUDA_SUCCESS ||
       encode_bhnd(encode, &maps[2], pr.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr) != CUDA_SUCCESS ||
-      encode_bhnd(encode, &maps[3], split ? klo : kbase, kdt, pr) != CUDA_SUCCESS ||
+      encode_bhnd(encode, &maps[3], split ? klo : kbase, kdt, pr, pair ? kBN / 2 : kBN) != CUDA_SUCCESS ||
       encode_bhnd(encode, &maps[4], split && q_pre ? qlo : qbase, qdt, pr) != CUDA_SUCCESS ||
       encode_bhnd(encode, &maps[5], pr.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr) != CUDA_SUCCESS) {
     *what = "cuTensorMapEncodeTiled failed";
     return cudaErrorInvalidValue;
   }
   if (fused) return launch_attn<kModeFused>(pr, p, maps, stream, what);
+  if (pair) return launch_attn<kModePair>(pr, p, maps, stream, what);
   if (split) return launch_attn<kModeSplit>(pr, p, maps, stream, what);
   return launch_attn<kModePrepass>(pr, p, maps, stream, what);
 }
