@@ -74,8 +74,9 @@ def _source_hash():
     return hashlib.sha256(src.encode()).hexdigest()[:16]
 
 
-def _traffic_per_launch(workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel."""
+def _traffic_per_launch(workload, kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel
+    (same source, same kernel variant, same workload)."""
     try:
         kv = {}
         with open(TRAFFIC_FILE) as f:
@@ -83,7 +84,8 @@ def _traffic_per_launch(workload):
                 if ":" in line and not line.startswith("#"):
                     key, val = line.split(":", 1)
                     kv[key.strip()] = val.strip()
-        if kv.get("kernel_source_sha256_16") != _source_hash() or kv.get("workload") != workload:
+        if (kv.get("kernel_source_sha256_16") != _source_hash() or kv.get("workload") != workload or
+                kv.get("kernel", "single") != kernel):
             return None
         return float(kv["dram_bytes_per_launch"])
     except Exception:
@@ -264,8 +266,9 @@ def cpu_baseline(w, q, k, v, min_seconds=8.0, max_samples=16):
             "kind": "oracle", "sample": _sample_text(w, n, total_s)}
 
 
-def _config(w, k_rope="prepass"):
-    return {"workload": w.name, "k_rope": k_rope, "qk_operands": w.qk, "B": w.B, "heads": w.H, "head_dim": w.d,
+def _config(w, k_rope="prepass", kernel="default"):
+    return {"workload": w.name, "k_rope": k_rope, "qk_operands": w.qk, "kernel": kernel, "B": w.B,
+            "heads": w.H, "head_dim": w.d,
             "grid": f"{w.T}x{w.Hg}x{w.Wg}", "N": w.N,
             "sections": "/".join(map(str, w.sections)), "theta": w.theta,
             "l2": _l2_note(w),
@@ -335,6 +338,15 @@ def _e2e_leg(w, q, k, v, out, lse, hq, hk, hv, call, stream, dev, barrier, max_o
                       "(double-buffered device inputs and outputs)"}
 
 
+def _kernel_used(args, w):
+    """Which attention kernel runs the timed calls (the library's default rule for dense calls:
+    CTA pairs for fp16 operands, the K prepass and N >= 65536)."""
+    if args.kernel != "default":
+        return args.kernel
+    dense = not args.window and not args.subset and args.k_rope == "prepass" and w.qk == "fp16"
+    return "pair" if dense and w.N >= 65536 else "single"
+
+
 def run_ours(args, w):
     import torch
     import video_diffusion_transformer_rope_gb300 as vdx
@@ -394,9 +406,11 @@ def run_ours(args, w):
             vdx.rope3d_attn_subset(qq, kk, vv, grid, idx, oo, ll, w.sections, w.theta,
                                    stream=stream, workspace=k_ws, qk_precision=qk)
     else:
+        kern = {"default": vdx.KERNEL_DEFAULT, "single": vdx.KERNEL_SINGLE, "pair": vdx.KERNEL_PAIR}[args.kernel]
+
         def call(qq, kk, vv, oo, ll):
             vdx.rope3d_attn(qq, kk, vv, grid, w.sections, w.theta, out=oo, lse=ll, stream=stream,
-                            k_rope=k_mode, workspace=k_ws, qk_precision=qk)
+                            k_rope=k_mode, workspace=k_ws, qk_precision=qk, kernel=kern)
 
     def step():
         call(q, k, v, out, lse)
@@ -446,7 +460,7 @@ def run_ours(args, w):
     tflops_rank = job_tflops(work, ms, 1)
     value = job_tflops(work, ms, ws)
     peak, peak_sus, peak_src = _peaks()
-    traffic = _traffic_per_launch(w.name)
+    traffic = _traffic_per_launch(w.name, _kernel_used(args, w))
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.window and not args.subset:
@@ -459,7 +473,7 @@ def run_ours(args, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) on device, bf16)",
-            "config": dict(_config(w, args.k_rope), **({"window": args.window,
+            "config": dict(_config(w, args.k_rope, _kernel_used(args, w)), **({"window": args.window,
                                                          "mask_density": work / w.flops}
                                                         if args.window else {}),
                            **({"active_query_fraction": float(args.subset)} if args.subset else {})),
@@ -469,8 +483,8 @@ def run_ours(args, w):
                          "frac": tflops_rank / peak, "traffic": traffic,
                          "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)",
                          "frac_of_sustained": (tflops_rank / peak_sus) if peak_sus else None,
-                         "kernel": "attn_fwd_sm103 (+ rope3d_qk_prepass)" if args.k_rope == "prepass"
-                         else "attn_fwd_sm103 (fused K rotation)"},
+                         "kernel": (f"attn_fwd_sm103, {_kernel_used(args, w)} (+ rope3d_qk_prepass)"
+                                    if args.k_rope == "prepass" else "attn_fwd_sm103 (fused K rotation)")},
             "cpu_baseline": cpu,
             "clocks": clocks,
         }
@@ -497,6 +511,9 @@ def main():
     ap.add_argument("--k-rope", choices=["prepass", "fused"], default="prepass",
                     help="K rotated once by a prepass kernel (default) or per tile inside the "
                          "attention kernel")
+    ap.add_argument("--kernel", choices=["default", "single", "pair"], default="default",
+                    help="attention kernel for dense calls: the library's choice, one CTA per 256 "
+                         "query rows, or CTA pairs sharing each K/V tile")
     ap.add_argument("--qk", choices=["fp16", "split"], default=None,
                     help="QK operand precision (default: the workload's own: split for the "
                          "long-clip stress workload, fp16 for the others)")
