@@ -340,10 +340,10 @@ def _e2e_leg(w, q, k, v, out, lse, hq, hk, hv, call, stream, dev, barrier, max_o
 
 def _kernel_used(args, w):
     """Which attention kernel runs the timed calls (the library's default rule for dense calls:
-    CTA pairs for fp16 operands, the K prepass and N >= 65536)."""
+    CTA pairs with the K prepass and N >= 65536)."""
     if args.kernel != "default":
         return args.kernel
-    dense = not args.window and not args.subset and args.k_rope == "prepass" and w.qk == "fp16"
+    dense = not args.window and not args.subset and args.k_rope == "prepass"
     return "pair" if dense and w.N >= 65536 else "single"
 
 

@@ -69,8 +69,7 @@ typedef enum {
 #define VDX_KERNEL_SINGLE 1   /* one CTA per 256 query rows, each streaming whole K/V tiles          */
 #define VDX_KERNEL_PAIR 2     /* clusters of two CTAs: each holds half of every K/V tile and the pair
                                  multiplies both CTAs' 512 query rows with CTA-pair MMAs; dense
-                                 calls with the K prepass and fp16 operands only (otherwise
-                                 VDX_ERR_UNSUPPORTED)                                            */
+                                 calls with the K prepass only (otherwise VDX_ERR_UNSUPPORTED)   */
 
 typedef struct vdx_attn_options {
   int k_rope;               /* one of VDX_K_ROPE_*                                              */

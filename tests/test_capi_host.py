@@ -116,7 +116,6 @@ def test_ex_rejects_bad_options(L):
 
 @pytest.mark.parametrize("k_rope,prec,kernel,status", [
     (_binding.K_ROPE_FUSED, _binding.QK_FP16, _binding.KERNEL_PAIR, _binding.VDX_ERR_UNSUPPORTED),
-    (_binding.K_ROPE_PREPASS, _binding.QK_SPLIT, _binding.KERNEL_PAIR, _binding.VDX_ERR_UNSUPPORTED),
     (_binding.K_ROPE_PREPASS, _binding.QK_FP16, 9, _binding.VDX_ERR_ARG),
 ])
 def test_ex_rejects_unsupported_kernel_choices(L, k_rope, prec, kernel, status):

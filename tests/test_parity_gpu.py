@@ -82,6 +82,15 @@ def test_bf16_cta_pair_small_shapes(grid):
     assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
 
 
+@pytest.mark.parametrize("grid", [(2, 9, 40), (1, 1, 129), (4, 9, 13)], ids=lambda g: "x".join(map(str, g)))
+def test_bf16_cta_pair_split_precision_stress_small(grid):
+    # the stress recipe with split operands, run by CTA pairs
+    w = dataclasses.replace(configs.LONG_STRESS, B=1, H=4, T=grid[0], Hg=grid[1], Wg=grid[2], seed=45)
+    assert w.qk == "split"
+    mx, mean, lerr = _full_compare(w, kernel=vdx.KERNEL_PAIR)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
+
+
 def test_bf16_cta_pair_agrees_with_single_cta_kernel():
     # same fp16 operands and softmax, different MMA shapes: equal to rounding
     w = dataclasses.replace(configs.WAN13B_480P, B=2, H=5, T=3, Hg=10, Wg=30, seed=44)
@@ -267,7 +276,8 @@ def test_full_size_configs_sampled(w):
     _assert_sampled(w, mx, mean, lerr, stats)
 
 
-@pytest.mark.parametrize("w", [configs.WAN13B_480P, configs.WAN14B_720P], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [configs.WAN13B_480P, configs.WAN14B_720P, configs.LONG_STRESS],
+                         ids=lambda w: w.name)
 def test_full_size_cta_pair_sampled(w):
     mx, mean, lerr, stats = _sampled_compare(w, kernel=vdx.KERNEL_PAIR)
     print(f"{w.name} (CTA pairs): out max {mx:.3e} mean {mean:.3e} lse max {lerr:.3e} {stats}")

@@ -91,16 +91,19 @@ constexpr int kMaxDynSmem = 232448;      // sm_100-family opt-in limit per CTA
 // K/V tile: each CTA holds half of it (keys 0-63 or 64-127 of a K tile, channels 0-63 or
 // 64-127 of a V tile) and the pair's rank-0 CTA issues cta_group::2 MMAs over both CTAs' 256
 // query rows.
-enum : int { kModePrepass = 0, kModeFused = 1, kModeSplit = 2, kModePair = 3 };
+// kModePairSplit: the split mode run by CTA pairs (each CTA: Q hi + lo, 2-stage rings of K
+// halves hi + lo and V halves).
+enum : int { kModePrepass = 0, kModeFused = 1, kModeSplit = 2, kModePair = 3, kModePairSplit = 4 };
 
 template <int kMode>
 struct Layout {
   static constexpr bool kFusedK = kMode == kModeFused;
-  static constexpr bool kSplit = kMode == kModeSplit;
-  static constexpr bool kPair = kMode == kModePair;
-  static constexpr int kKStages = kMode == kModePrepass ? 3 : (kMode == kModeFused ? 2 : (kPair ? 4 : 1));
-  static constexpr int kVStages = kSplit ? 1 : (kPair ? 4 : 2);
-  static constexpr int kKStageBytes = kSplit ? 2 * kTileBytes : (kPair ? kTileBytes / 2 : kTileBytes);   // hi [+ lo]
+  static constexpr bool kSplit = kMode == kModeSplit || kMode == kModePairSplit;
+  static constexpr bool kPair = kMode == kModePair || kMode == kModePairSplit;
+  static constexpr int kKStages = kMode == kModePrepass ? 3 : (kMode == kModeFused ? 2 : (kMode == kModePair ? 4 : (kMode == kModePairSplit ? 2 : 1)));
+  static constexpr int kVStages = kMode == kModeSplit ? 1 : (kMode == kModePair ? 4 : 2);
+  // K stage: one tile (hi), or hi + lo; a CTA pair holds half of each
+  static constexpr int kKStageBytes = (kSplit ? 2 * kTileBytes : kTileBytes) / (kPair ? 2 : 1);
   static constexpr int kVStageBytes = kPair ? kTileBytes / 2 : kTileBytes;
   static constexpr int kOffQ = 0;                                              // Q (hi) tiles
   static constexpr int kOffQlo = kOffQ + kQTiles * kTileBytes;                 // Q lo tiles
@@ -274,13 +277,13 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
 // memory, B = V with channels 0-63 in rank 0's stage and 64-127 in rank 1's (128 keys x 128
 // bytes each, MN-major).  M = 256, N = 128 in both.
 __device__ __forceinline__ void issue_qk_pair(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
-                                              uint32_t idesc) {
+                                              uint32_t idesc, bool accumulate = false) {
 #pragma unroll
   for (int kk = 0; kk < kD / 16; ++kk) {
     const uint32_t a_off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
     const uint32_t b_off = (kk >> 2) * (kHalfBytes / 2) + (kk & 3) * 32;
     mma_ss_pair_warp(d_tmem, smem_desc_sw128(a_smem + a_off, 16, 1024),
-                     smem_desc_sw128(b_smem + b_off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+                     smem_desc_sw128(b_smem + b_off, 16, 1024), idesc, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 __device__ __forceinline__ void issue_pv_pair(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
@@ -563,13 +566,17 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (ku > 0 && !mbar_wait(smem_addr(&ctl->k_empty[ks]), (ku - 1) & 1, abort_flag, kSiteKEmpty))
           break;
         if constexpr (kPair) {
-          // this CTA's 64 keys of the tile (tm_klo holds the 64-token-box map of K here)
+          // this CTA's 64 keys of the tile (the K maps have 64-token boxes here): hi, then lo
           const uint32_t bar = smem_addr(&ctl->k_full[ks]);
           mbar_arrive_expect_tx(bar, Lo::kKStageBytes);
           const uint32_t dst = sK + ks * Lo::kKStageBytes;
           const int row = kt * kBN + static_cast<int>(rank) * (kBN / 2);
-          tma_load_4d(dst, &tm_klo, bar, 0, h, row, b);
-          tma_load_4d(dst + kHalfBytes / 2, &tm_klo, bar, 64, h, row, b);
+          tma_load_4d(dst, &tm_k, bar, 0, h, row, b);
+          tma_load_4d(dst + kHalfBytes / 2, &tm_k, bar, 64, h, row, b);
+          if (kSplit) {
+            tma_load_4d(dst + kTileBytes / 2, &tm_klo, bar, 0, h, row, b);
+            tma_load_4d(dst + kTileBytes / 2 + kHalfBytes / 2, &tm_klo, bar, 64, h, row, b);
+          }
           k_issued = j + 1;
         } else {
           const uint32_t bar = smem_addr(&ctl->k_full[ks]);
@@ -629,7 +636,12 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int ks = j % kKStages;
         tc_fence_after_sync();
         const uint32_t kst = sK + ks * Lo::kKStageBytes;
+        const uint32_t sQlo = smem_addr(smem + Lo::kOffQlo);
         issue_qk_pair(tS0, sQ, kst, kIdQK);
+        if (kSplit) {
+          issue_qk_pair(tS0, sQ, kst + kTileBytes / 2, kIdQK, true);     // Qhi Klo
+          issue_qk_pair(tS0, sQlo, kst, kIdQK, true);                    // Qlo Khi
+        }
         mma_commit_pair_warp(smem_addr(&ctl->s_full[0]));
         if (j > 0) {
           ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->p_ready[1]), (j - 1) & 1, abort_flag,
@@ -641,6 +653,10 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           mma_commit_pair_warp(smem_addr(&ctl->v_empty[pvs]));
         }
         issue_qk_pair(tS1, sQ + kTileBytes, kst, kIdQK);
+        if (kSplit) {
+          issue_qk_pair(tS1, sQ + kTileBytes, kst + kTileBytes / 2, kIdQK, true);
+          issue_qk_pair(tS1, sQlo + kTileBytes, kst, kIdQK, true);
+        }
         mma_commit_pair_warp(smem_addr(&ctl->s_full[1]));
         mma_commit_pair_warp(smem_addr(&ctl->k_empty[ks]));
         const int vs = j % kVStages;
@@ -1091,8 +1107,8 @@ cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, KMod
   fill_params(pr, &p);
   CUtensorMap maps[6];
   const bool fused = mode == KMode::kFused;
-  const bool split = mode == KMode::kSplit;
-  const bool pair = mode == KMode::kPair;
+  const bool split = mode == KMode::kSplit || mode == KMode::kPairSplit;
+  const bool pair = mode == KMode::kPair || mode == KMode::kPairSplit;
   if (pair) {
     if (pr.q_index != nullptr || pr.kv_mask != nullptr) {
       *what = "CTA pairs take dense calls only";
@@ -1146,7 +1162,7 @@ cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, KMod
   const CUtensorMapDataType kdt = fused ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const CUtensorMapDataType qdt = q_pre ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (encode_bhnd(encode, &maps[0], qbase, qdt, pr) != CUDA_SUCCESS ||
-      encode_bhnd(encode, &maps[1], kbase, kdt, pr) != CUDA_SUCCESS ||
+      encode_bhnd(encode, &maps[1], kbase, kdt, pr, pair ? kBN / 2 : kBN) != CUDA_SUCCESS ||
       encode_bhnd(encode, &maps[2], pr.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pr) != CUDA_SUCCESS ||
       encode_bhnd(encode, &maps[3], split ? klo : kbase, kdt, pr, pair ? kBN / 2 : kBN) != CUDA_SUCCESS ||
       encode_bhnd(encode, &maps[4], split && q_pre ? qlo : qbase, qdt, pr) != CUDA_SUCCESS ||
@@ -1155,6 +1171,7 @@ cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, KMod
     return cudaErrorInvalidValue;
   }
   if (fused) return launch_attn<kModeFused>(pr, p, maps, stream, what);
+  if (pair && split) return launch_attn<kModePairSplit>(pr, p, maps, stream, what);
   if (pair) return launch_attn<kModePair>(pr, p, maps, stream, what);
   if (split) return launch_attn<kModeSplit>(pr, p, maps, stream, what);
   return launch_attn<kModePrepass>(pr, p, maps, stream, what);

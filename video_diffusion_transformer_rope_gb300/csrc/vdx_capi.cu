@@ -222,15 +222,17 @@ static vdx_status attn_bf16(const void* q, const void* k, const void* v, void* o
   const int kernel = opt ? opt->kernel : VDX_KERNEL_DEFAULT;
   if (kernel != VDX_KERNEL_DEFAULT && kernel != VDX_KERNEL_SINGLE && kernel != VDX_KERNEL_PAIR)
     return fail(VDX_ERR_ARG, "unknown kernel %d", kernel);
-  if (kernel == VDX_KERNEL_PAIR && (fused || split || block_mask || q_index))
-    return fail(VDX_ERR_UNSUPPORTED, "VDX_KERNEL_PAIR takes dense calls with the K prepass and fp16 operands only");
+  if (kernel == VDX_KERNEL_PAIR && (fused || block_mask || q_index))
+    return fail(VDX_ERR_UNSUPPORTED, "VDX_KERNEL_PAIR takes dense calls with the K prepass only");
   // CTA pairs by default for long dense sequences (N >= 65536, >= 512 key tiles per CTA): at
   // the same power they run ~7 % higher clocks (half the shared-memory operand reads and L2->SM
   // traffic per CTA), which outweighs their longer cross-SM signalling there (+0.8 % at N =
-  // 75600); at N = 32760 they measured -1.8 % to +0.2 %, so shorter sequences keep one CTA.
+  // 75600 with fp16 operands; +16 % with split operands, where halving each CTA's K/V stages
+  // lets its rings hold two stages instead of one); at N = 32760 with fp16 operands they
+  // measured -1.8 % to +0.2 %, so shorter sequences keep one CTA.
   const long long n_tokens = static_cast<long long>(T) * Hgrid * Wgrid;
   const bool pair = kernel == VDX_KERNEL_PAIR ||
-                    (kernel == VDX_KERNEL_DEFAULT && !fused && !split && !block_mask && !q_index &&
+                    (kernel == VDX_KERNEL_DEFAULT && !fused && !block_mask && !q_index &&
                      n_tokens >= 65536);
   if (fused && split)
     return fail(VDX_ERR_UNSUPPORTED, "VDX_QK_SPLIT needs the K prepass (k_rope = VDX_K_ROPE_PREPASS)");
@@ -284,7 +286,8 @@ static vdx_status attn_bf16(const void* q, const void* k, const void* v, void* o
   if ((s = get_encode(&enc)) != VDX_OK) return s;
   const char* what = nullptr;
   const vdx::KMode km = fused ? vdx::KMode::kFused
-                              : (split ? vdx::KMode::kSplit : (pair ? vdx::KMode::kPair : vdx::KMode::kPrepass));
+                              : (split ? (pair ? vdx::KMode::kPairSplit : vdx::KMode::kSplit)
+                                       : (pair ? vdx::KMode::kPair : vdx::KMode::kPrepass));
   cudaError_t e = vdx::launch_attn_bf16_sm103(p, enc, km, ws, q_pre, static_cast<cudaStream_t>(stream),
                                               &what);
   if (e != cudaSuccess)

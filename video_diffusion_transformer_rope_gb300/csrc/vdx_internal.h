@@ -47,10 +47,11 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 //             both) and three QK products.
 //   kPair:    as kPrepass, run by clusters of two CTAs that split every K/V tile between them
 //             and multiply both CTAs' query rows with one cta_group::2 MMA (dense calls only).
+//   kPairSplit: kSplit run by CTA pairs.
 // With rotate_q_in_prepass (kPrepass / kSplit, no query subset) the prepass also rotates Q
 // (multiplied by scale*log2(e)) into the workspace after K, and the attention kernel loads
 // it rotated; otherwise every CTA rotates its Q tiles in shared memory.
-enum class KMode { kPrepass, kFused, kSplit, kPair };
+enum class KMode { kPrepass, kFused, kSplit, kPair, kPairSplit };
 cudaError_t launch_attn_bf16_sm103(const Problem& p, EncodeTiledFn encode, KMode mode,
                                    void* workspace, bool rotate_q_in_prepass, cudaStream_t stream,
                                    const char** what);
