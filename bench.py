@@ -339,12 +339,12 @@ def _e2e_leg(w, q, k, v, out, lse, hq, hk, hv, call, stream, dev, barrier, max_o
 
 
 def _kernel_used(args, w):
-    """Which attention kernel runs the timed calls (the library's default rule for dense calls:
-    CTA pairs with the K prepass and N >= 65536)."""
+    """Which attention kernel runs the timed calls (the library's default rule for dense calls
+    with the K prepass: CTA pairs for split operands, or for fp16 operands with N >= 65536)."""
     if args.kernel != "default":
         return args.kernel
     dense = not args.window and not args.subset and args.k_rope == "prepass"
-    return "pair" if dense and w.N >= 65536 else "single"
+    return "pair" if dense and (w.qk == "split" or w.N >= 65536) else "single"
 
 
 def run_ours(args, w):

@@ -101,12 +101,13 @@ def test_bf16_cta_pair_agrees_with_single_cta_kernel():
     assert (l1 - l2).abs().max().item() <= 1e-4
 
 
+@pytest.mark.parametrize("kernel", ["single", "pair"])
 @pytest.mark.parametrize("grid", [(3, 8, 8), (1, 1, 129), (4, 9, 13), (7, 40, 1)],
                          ids=lambda g: "x".join(map(str, g)))
-def test_bf16_split_precision_small_shapes(grid):
+def test_bf16_split_precision_small_shapes(grid, kernel):
     w = dataclasses.replace(configs.WAN13B_480P, B=2, H=3, T=grid[0], Hg=grid[1], Wg=grid[2], seed=26,
                             qk="split")
-    mx, mean, lerr = _full_compare(w)
+    mx, mean, lerr = _full_compare(w, kernel=vdx.KERNEL_PAIR if kernel == "pair" else vdx.KERNEL_SINGLE)
     # hi + lo operands: the score error is far below fp16's, so lse is far inside its tolerance
     assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL / 10, (mx, mean, lerr)
 
@@ -276,11 +277,14 @@ def test_full_size_configs_sampled(w):
     _assert_sampled(w, mx, mean, lerr, stats)
 
 
-@pytest.mark.parametrize("w", [configs.WAN13B_480P, configs.WAN14B_720P, configs.LONG_STRESS],
-                         ids=lambda w: w.name)
-def test_full_size_cta_pair_sampled(w):
-    mx, mean, lerr, stats = _sampled_compare(w, kernel=vdx.KERNEL_PAIR)
-    print(f"{w.name} (CTA pairs): out max {mx:.3e} mean {mean:.3e} lse max {lerr:.3e} {stats}")
+# The other kernel than the default at full size: CTA pairs where one CTA is the default
+# (N < 65536), one CTA where pairs are.
+@pytest.mark.parametrize("w,kernel", [(configs.WAN13B_480P, "pair"), (configs.WAN14B_720P, "single"),
+                                      (configs.LONG_STRESS, "single")], ids=lambda x: getattr(x, "name", x))
+def test_full_size_other_kernel_sampled(w, kernel):
+    kern = vdx.KERNEL_PAIR if kernel == "pair" else vdx.KERNEL_SINGLE
+    mx, mean, lerr, stats = _sampled_compare(w, kernel=kern)
+    print(f"{w.name} ({kernel}): out max {mx:.3e} mean {mean:.3e} lse max {lerr:.3e} {stats}")
     _assert_sampled(w, mx, mean, lerr, stats)
 
 

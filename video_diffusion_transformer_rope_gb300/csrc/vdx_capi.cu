@@ -224,16 +224,16 @@ static vdx_status attn_bf16(const void* q, const void* k, const void* v, void* o
     return fail(VDX_ERR_ARG, "unknown kernel %d", kernel);
   if (kernel == VDX_KERNEL_PAIR && (fused || block_mask || q_index))
     return fail(VDX_ERR_UNSUPPORTED, "VDX_KERNEL_PAIR takes dense calls with the K prepass only");
-  // CTA pairs by default for long dense sequences (N >= 65536, >= 512 key tiles per CTA): at
-  // the same power they run ~7 % higher clocks (half the shared-memory operand reads and L2->SM
-  // traffic per CTA), which outweighs their longer cross-SM signalling there (+0.8 % at N =
-  // 75600 with fp16 operands; +16 % with split operands, where halving each CTA's K/V stages
-  // lets its rings hold two stages instead of one); at N = 32760 with fp16 operands they
-  // measured -1.8 % to +0.2 %, so shorter sequences keep one CTA.
+  // CTA pairs by default for dense calls with split operands (halving each CTA's K/V stages
+  // lets its rings hold two stages instead of one: +16 % at N = 111600, +20 % at N = 32760)
+  // and for long dense sequences with fp16 operands (N >= 65536, >= 512 key tiles per CTA): at
+  // the same power pairs run ~7 % higher clocks (half the shared-memory operand reads and
+  // L2->SM traffic per CTA), which outweighs their longer cross-SM signalling there (+0.8 % at
+  // N = 75600); at N = 32760 they measured -1.8 % to +0.2 %, so shorter fp16 calls keep one CTA.
   const long long n_tokens = static_cast<long long>(T) * Hgrid * Wgrid;
   const bool pair = kernel == VDX_KERNEL_PAIR ||
                     (kernel == VDX_KERNEL_DEFAULT && !fused && !block_mask && !q_index &&
-                     n_tokens >= 65536);
+                     (split || n_tokens >= 65536));
   if (fused && split)
     return fail(VDX_ERR_UNSUPPORTED, "VDX_QK_SPLIT needs the K prepass (k_rope = VDX_K_ROPE_PREPASS)");
   vdx::Problem p{};
