@@ -677,6 +677,10 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       mma_commit_pair_warp(smem_addr(&ctl->o_final));
       drain_wait(smem_addr(&ctl->o_final), 0);
+    } else if (kPair && warp == 13 && !leader) {
+      // rank 1: the leader's final commit also arrives here; see it land before this CTA can
+      // retire (the softmax warps skip their wait for it after an abort)
+      drain_wait(smem_addr(&ctl->o_final), 0);
     } else if (kPair && warp == 14 && lane == 0 && !leader) {
       // ---------------------------------------------------------- relay (rank 1 of a pair):
       // tells the leader, through one remote arrival per phase, that this CTA's Q tiles and
