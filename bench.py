@@ -293,15 +293,21 @@ def _e2e_leg(w, q, k, v, out, lse, hq, hk, hv, call, stream, dev, barrier, max_o
     computed = [torch.cuda.Event() for _ in range(2)]
     drained = [torch.cuda.Event() for _ in range(2)]
     e2e_steps = max(1, steps)
+    # per-step timestamps on each stream (read after the timed region) to show how far the
+    # copies overlapped the kernels
+    mark = {k: [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+            for k in ("up0", "up1", "run0", "run1", "down0", "down1")}
 
     def upload(i):
         sl = i % 2
         with torch.cuda.stream(s_in):
             if i >= 2:
                 s_in.wait_event(computed[sl])          # the kernel that read this slot is done
+            mark["up0"][i].record(s_in)
             dq[sl].copy_(hq, non_blocking=True)
             dk[sl].copy_(hk, non_blocking=True)
             dv[sl].copy_(hv, non_blocking=True)
+            mark["up1"][i].record(s_in)
             in_ready[sl].record(s_in)
 
     barrier()
@@ -316,12 +322,16 @@ def _e2e_leg(w, q, k, v, out, lse, hq, hk, hv, call, stream, dev, barrier, max_o
         stream.wait_event(in_ready[sl])
         if i >= 2:
             stream.wait_event(drained[sl])             # this slot's previous result is home
+        mark["run0"][i].record(stream)
         call(dq[sl], dk[sl], dv[sl], dout[sl], dlse[sl])
+        mark["run1"][i].record(stream)
         computed[sl].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(computed[sl])
+            mark["down0"][i].record(s_out)
             hout[sl].copy_(dout[sl], non_blocking=True)
             hlse[sl].copy_(dlse[sl], non_blocking=True)
+            mark["down1"][i].record(s_out)
             drained[sl].record(s_out)
     stream.wait_stream(s_in)
     stream.wait_stream(s_out)
@@ -332,8 +342,14 @@ def _e2e_leg(w, q, k, v, out, lse, hq, hk, hv, call, stream, dev, barrier, max_o
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = hout[0].numel() * hout[0].element_size() + hlse[0].numel() * hlse[0].element_size()
 
+    mean = lambda a, b: statistics.mean(mark[a][i].elapsed_time(mark[b][i]) for i in range(e2e_steps))
+    streams = {"upload_ms": mean("up0", "up1"), "kernels_ms": mean("run0", "run1"),
+               "download_ms": mean("down0", "down1")}
+    streams["upload_gbs"] = h2d / streams["upload_ms"] / 1e6
+    streams["download_gbs"] = d2h / streams["download_ms"] / 1e6
     return {"value": job_tflops(work, e2e_ms, ws), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
+            "per_stream_mean": streams,
             "copies": "pinned host memory, H2D and D2H streams overlapping compute "
                       "(double-buffered device inputs and outputs)"}
 
