@@ -32,7 +32,8 @@
 // Split (precise): as prepass, but every rotated Q/K value x is kept as two fp16 numbers,
 // hi = fp16(x) and lo = fp16(x - hi), and S = Qhi Khi^T + Qhi Klo^T + Qlo Khi^T (about 22
 // significant bits per operand instead of 11) for inputs whose logits reach the hundreds.
-// Three QK products and one-stage K/V rings (shared memory holds Q hi+lo and K hi+lo).
+// Three QK products and one-stage K/V rings (shared memory holds Q hi+lo and K hi+lo); run by
+// CTA pairs (below), each CTA holds half of every K/V tile and its rings hold two stages.
 //
 // CTA pairs (long dense sequences): two CTAs of a cluster take consecutive query blocks of one
 // (b, h).  Each loads only half of every K tile (keys 0-63 or 64-127) and half of every V tile
