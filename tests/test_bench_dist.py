@@ -45,3 +45,21 @@ def test_two_gloo_replicas_aggregate():
 def test_single_rank_is_identity():
     assert bench.reduce_max_over_ranks(3.5, 1, torch.device("cpu")) == 3.5
     assert bench.job_tflops(1e12, 1000.0, 1) == pytest.approx(1.0)
+
+
+def test_kernel_choice_and_stored_traffic_follow_the_library_rule():
+    # bench.py names the attention kernel a run uses with the library's default rule (CTA pairs
+    # for split operands, or for fp16 operands with N >= 65536) and reports the stored DRAM
+    # traffic only for the kernel variant and workload it was captured on.
+    import argparse
+    from video_diffusion_transformer_rope_gb300 import configs
+    args = argparse.Namespace(kernel="default", window=None, subset=None, k_rope="prepass")
+    assert bench._kernel_used(args, configs.WAN14B_720P) == "pair"
+    assert bench._kernel_used(args, configs.LONG_STRESS) == "pair"
+    assert bench._kernel_used(args, configs.WAN13B_480P) == "single"
+    assert bench._kernel_used(argparse.Namespace(**{**vars(args), "window": "2,6,10"}), configs.WAN14B_720P) == "single"
+    assert bench._kernel_used(argparse.Namespace(**{**vars(args), "kernel": "single"}), configs.WAN14B_720P) == "single"
+    t = bench._traffic_per_launch("wan14b_720p", "pair")
+    assert t is None or 6.2e9 <= t <= 9e9          # algorithmic bytes are 6.22 GB per launch
+    assert bench._traffic_per_launch("wan14b_720p", "single") is None
+    assert bench._traffic_per_launch("wan1.3b_480p", "pair") is None
