@@ -69,7 +69,9 @@ typedef enum {
 #define VDX_KERNEL_SINGLE 1   /* one CTA per 256 query rows, each streaming whole K/V tiles          */
 #define VDX_KERNEL_PAIR 2     /* clusters of two CTAs: each holds half of every K/V tile and the pair
                                  multiplies both CTAs' 512 query rows with CTA-pair MMAs; dense
-                                 calls with the K prepass only (otherwise VDX_ERR_UNSUPPORTED)   */
+                                 calls only (block-sparse and query-subset calls get
+                                 VDX_ERR_UNSUPPORTED).  With VDX_K_ROPE_FUSED each CTA rotates
+                                 its own Q tiles and its 64 keys of every K tile                */
 
 typedef struct vdx_attn_options {
   int k_rope;               /* one of VDX_K_ROPE_*                                              */

@@ -115,15 +115,31 @@ def test_ex_rejects_bad_options(L):
 
 
 @pytest.mark.parametrize("k_rope,prec,kernel,status", [
-    (_binding.K_ROPE_FUSED, _binding.QK_FP16, _binding.KERNEL_PAIR, _binding.VDX_ERR_UNSUPPORTED),
     (_binding.K_ROPE_PREPASS, _binding.QK_FP16, 9, _binding.VDX_ERR_ARG),
+    (_binding.K_ROPE_FUSED, _binding.QK_FP16, -1, _binding.VDX_ERR_ARG),
 ])
-def test_ex_rejects_unsupported_kernel_choices(L, k_rope, prec, kernel, status):
+def test_ex_rejects_unknown_kernel_choices(L, k_rope, prec, kernel, status):
     opt = _binding.AttnOptions(k_rope, prec, None, 0, 0, kernel)
     r = L.vdx_rope3d_attn_ex(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + (1 << 32)),
                              ctypes.c_void_p(FAKE + (2 << 32)), ctypes.c_void_p(FAKE + (3 << 32)),
                              None, 1, 2, 2, 3, 4, 128, 0, 0, 0, 10000.0, 0.0, ctypes.byref(opt), None)
     assert r == status and "kernel" in L.vdx_last_error().decode().lower()
+
+
+def test_sparse_and_subset_calls_reject_cta_pairs(L):
+    # CTA pairs take dense calls only (with either K rotation); a block mask or a query subset
+    # with VDX_KERNEL_PAIR is refused before any device work.
+    opt = _binding.AttnOptions(_binding.K_ROPE_PREPASS, _binding.QK_FP16, None, 0, 0, _binding.KERNEL_PAIR)
+    r = L.vdx_rope3d_attn_sparse(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + (1 << 32)),
+                                 ctypes.c_void_p(FAKE + (2 << 32)), ctypes.c_void_p(FAKE + (3 << 32)),
+                                 None, 1, 2, 2, 3, 4, 128, 0, 0, 0, 10000.0, 0.0,
+                                 ctypes.c_void_p(FAKE + (4 << 32)), 0, ctypes.byref(opt), None)
+    assert r == _binding.VDX_ERR_UNSUPPORTED and "dense" in L.vdx_last_error().decode()
+    r = L.vdx_rope3d_attn_subset(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + (1 << 32)),
+                                 ctypes.c_void_p(FAKE + (2 << 32)), ctypes.c_void_p(FAKE + (3 << 32)),
+                                 None, 1, 2, 2, 3, 4, 128, 0, 0, 0, 10000.0, 0.0,
+                                 ctypes.c_void_p(FAKE + (4 << 32)), 8, 0, ctypes.byref(opt), None)
+    assert r == _binding.VDX_ERR_UNSUPPORTED and "dense" in L.vdx_last_error().decode()
 
 
 def test_python_binding_rejects_mismatched_grid(L):

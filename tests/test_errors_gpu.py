@@ -47,7 +47,7 @@ def test_bad_arguments_raise_before_launch():
     vdx.sync_check()
 
 
-@pytest.mark.parametrize("kernel", ["single", "pair"])
+@pytest.mark.parametrize("kernel", ["single", "pair", "pair_fused"])
 def test_pipeline_wait_timeout_is_reported_and_context_stays_usable(kernel):
     # The producer withholds every K/V tile: the MMA and softmax waits run out after ~1 s, the
     # kernel stops cleanly (TMEM freed, its own copies drained), and the status says so.  With
@@ -57,8 +57,9 @@ def test_pipeline_wait_timeout_is_reported_and_context_stays_usable(kernel):
     w = dataclasses.replace(configs.WAN13B_480P, B=1, H=1, T=1, Hg=2, Wg=64, seed=32)
     q, k, v = (t.cuda() for t in synth.make_qkv(w))
     out = torch.empty_like(q)
-    opt = _binding.AttnOptions(vdx.K_ROPE_PREPASS, vdx.QK_FP16, None, 0, 1,
-                               vdx.KERNEL_PAIR if kernel == "pair" else vdx.KERNEL_SINGLE)
+    opt = _binding.AttnOptions(vdx.K_ROPE_FUSED if kernel == "pair_fused" else vdx.K_ROPE_PREPASS,
+                               vdx.QK_FP16, None, 0, 1,
+                               vdx.KERNEL_SINGLE if kernel == "single" else vdx.KERNEL_PAIR)
     L = vdx.lib()
     st = L.vdx_rope3d_attn_ex(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
                               ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()), None,

@@ -73,12 +73,14 @@ def test_bf16_small_shapes(grid, mode):
 
 
 # CTA pairs: N = 192 and 129 (one query block, so a padding CTA completes the pair), 468, 640
-# (three blocks: padded to four), 1 (a single token), 280 (T = 7, Wg = 1).
+# (three blocks: padded to four), 1 (a single token), 280 (T = 7, Wg = 1).  With the fused K
+# rotation each CTA rotates its own Q tiles and its 64 keys of every K tile.
+@pytest.mark.parametrize("mode", sorted(K_MODES))
 @pytest.mark.parametrize("grid", [(3, 8, 8), (1, 1, 129), (4, 9, 13), (5, 8, 16), (1, 1, 1), (7, 40, 1)],
                          ids=lambda g: "x".join(map(str, g)))
-def test_bf16_cta_pair_small_shapes(grid):
+def test_bf16_cta_pair_small_shapes(grid, mode):
     w = dataclasses.replace(configs.WAN13B_480P, B=2, H=3, T=grid[0], Hg=grid[1], Wg=grid[2], seed=43)
-    mx, mean, lerr = _full_compare(w, kernel=vdx.KERNEL_PAIR)
+    mx, mean, lerr = _full_compare(w, kernel=vdx.KERNEL_PAIR, k_rope=K_MODES[mode])
     assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
 
 
@@ -91,12 +93,14 @@ def test_bf16_cta_pair_split_precision_stress_small(grid):
     assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
 
 
-def test_bf16_cta_pair_agrees_with_single_cta_kernel():
-    # same fp16 operands and softmax, different MMA shapes: equal to rounding
+@pytest.mark.parametrize("mode", sorted(K_MODES))
+def test_bf16_cta_pair_agrees_with_single_cta_kernel(mode):
+    # same fp16 operands (up to the rounding of the rotation angles in the fused mode) and
+    # softmax, different MMA shapes: equal to rounding
     w = dataclasses.replace(configs.WAN13B_480P, B=2, H=5, T=3, Hg=10, Wg=30, seed=44)
     q, k, v = (t.cuda() for t in synth.make_qkv(w))
-    o1, l1 = _run(w, q, k, v, kernel=vdx.KERNEL_SINGLE)
-    o2, l2 = _run(w, q, k, v, kernel=vdx.KERNEL_PAIR)
+    o1, l1 = _run(w, q, k, v, kernel=vdx.KERNEL_SINGLE, k_rope=K_MODES[mode])
+    o2, l2 = _run(w, q, k, v, kernel=vdx.KERNEL_PAIR, k_rope=K_MODES[mode])
     assert (o1.float() - o2.float()).abs().max().item() <= 2e-3
     assert (l1 - l2).abs().max().item() <= 1e-4
 
@@ -149,11 +153,15 @@ def test_bf16_many_heads_several_waves(grid):
     assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
 
 
-def test_bf16_custom_sections_theta_scale():
+# the fused mode run by CTA pairs takes its rotation angles from per-pair frequencies instead
+# of the cos/sin table, so custom sections and theta go through both
+@pytest.mark.parametrize("kw", [{}, {"k_rope": vdx.K_ROPE_FUSED, "kernel": vdx.KERNEL_PAIR}],
+                         ids=["default", "fused_pair"])
+def test_bf16_custom_sections_theta_scale(kw):
     w = dataclasses.replace(configs.WAN13B_480P, B=1, H=2, T=3, Hg=6, Wg=20, sections=(64, 32, 32),
                             theta=500.0, seed=22)
     q, k, v = (t.cuda() for t in synth.make_qkv(w))
-    out, lse = vdx.rope3d_attn(q, k, v, (3, 6, 20), w.sections, w.theta, scale=0.05)
+    out, lse = vdx.rope3d_attn(q, k, v, (3, 6, 20), w.sections, w.theta, scale=0.05, **kw)
     vdx.sync_check()
     ref_o, ref_l = O.rope3d_attention(q, k, v, (3, 6, 20), w.sections, w.theta, scale=0.05)
     assert np.abs(out.double().cpu().numpy() - ref_o).max() <= BF16_MAX
@@ -288,19 +296,23 @@ def test_full_size_other_kernel_sampled(w, kernel):
     _assert_sampled(w, mx, mean, lerr, stats)
 
 
-def test_full_size_fused_k_mode_sampled():
-    w = configs.WAN13B_480P
-    mx, mean, lerr, stats = _sampled_compare(w, k_rope=vdx.K_ROPE_FUSED)
-    print(f"{w.name}: out max {mx:.3e} mean {mean:.3e} lse max {lerr:.3e} {stats}")
+@pytest.mark.parametrize("w,kernel", [(configs.WAN13B_480P, "single"), (configs.WAN14B_720P, "pair")],
+                         ids=lambda x: getattr(x, "name", x))
+def test_full_size_fused_k_mode_sampled(w, kernel):
+    kern = vdx.KERNEL_PAIR if kernel == "pair" else vdx.KERNEL_SINGLE
+    mx, mean, lerr, stats = _sampled_compare(w, k_rope=vdx.K_ROPE_FUSED, kernel=kern)
+    print(f"{w.name} (fused, {kernel}): out max {mx:.3e} mean {mean:.3e} lse max {lerr:.3e} {stats}")
     _assert_sampled(w, mx, mean, lerr, stats)
 
 
 @pytest.mark.parametrize("sections,theta", [((128, 0, 0), 10000.0), ((0, 64, 64), 10000.0),
                                             ((44, 42, 42), 1.0e6), ((2, 2, 124), 2.0)])
-def test_bf16_degenerate_sections_and_theta(sections, theta):
+@pytest.mark.parametrize("kw", [{}, {"k_rope": vdx.K_ROPE_FUSED, "kernel": vdx.KERNEL_PAIR}],
+                         ids=["default", "fused_pair"])
+def test_bf16_degenerate_sections_and_theta(sections, theta, kw):
     w = dataclasses.replace(configs.WAN13B_480P, B=1, H=2, T=3, Hg=7, Wg=11, seed=28,
                             sections=sections, theta=theta)
-    mx, mean, lerr = _full_compare(w)
+    mx, mean, lerr = _full_compare(w, **kw)
     assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
 
 
@@ -320,11 +332,12 @@ def test_bf16_uniform_attention_closed_form(which):
 
 
 @pytest.mark.parametrize("grid", [(1, 255, 128), (1, 1, 32641)], ids=["N_multiple_of_128", "N_one_past"])
-@pytest.mark.parametrize("k_rope", ["prepass", "fused"])
+@pytest.mark.parametrize("k_rope", ["prepass", "fused", "fused_pair"])
 def test_long_rows_with_and_without_a_ragged_tile(grid, k_rope):
     # N = 255*128 (no ragged key tile) and N = 256*128 + 1 (a last tile of one key); the prepass
     # mode rotates Q in the prepass, the fused mode in every CTA.
     w = dataclasses.replace(configs.WAN13B_480P, B=1, H=2, T=grid[0], Hg=grid[1], Wg=grid[2], seed=34)
-    kw = {} if k_rope == "prepass" else {"k_rope": vdx.K_ROPE_FUSED}
+    kw = {"prepass": {}, "fused": {"k_rope": vdx.K_ROPE_FUSED},
+          "fused_pair": {"k_rope": vdx.K_ROPE_FUSED, "kernel": vdx.KERNEL_PAIR}}[k_rope]
     mx, mean, lerr, stats = _sampled_compare(w, rows=256, **kw)
     _assert_sampled(w, mx, mean, lerr, stats)

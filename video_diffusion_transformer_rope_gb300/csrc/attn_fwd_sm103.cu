@@ -94,15 +94,23 @@ constexpr int kMaxDynSmem = 232448;      // sm_100-family opt-in limit per CTA
 // query rows.
 // kModePairSplit: the split mode run by CTA pairs (each CTA: Q hi + lo, 2-stage rings of K
 // halves hi + lo and V halves).
-enum : int { kModePrepass = 0, kModeFused = 1, kModeSplit = 2, kModePair = 3, kModePairSplit = 4 };
+// kModePairFused: the fused-K mode run by CTA pairs: each CTA rotates its own two Q tiles and
+// its half (64 keys) of every K tile in shared memory, so the per-CTA rotation work is half
+// that of kModeFused.
+enum : int {
+  kModePrepass = 0, kModeFused = 1, kModeSplit = 2, kModePair = 3, kModePairSplit = 4, kModePairFused = 5
+};
 
 template <int kMode>
 struct Layout {
-  static constexpr bool kFusedK = kMode == kModeFused;
+  static constexpr bool kFusedK = kMode == kModeFused || kMode == kModePairFused;
   static constexpr bool kSplit = kMode == kModeSplit || kMode == kModePairSplit;
-  static constexpr bool kPair = kMode == kModePair || kMode == kModePairSplit;
-  static constexpr int kKStages = kMode == kModePrepass ? 3 : (kMode == kModeFused ? 2 : (kMode == kModePair ? 4 : (kMode == kModePairSplit ? 2 : 1)));
-  static constexpr int kVStages = kMode == kModeSplit ? 1 : (kMode == kModePair ? 4 : 2);
+  static constexpr bool kPair = kMode == kModePair || kMode == kModePairSplit || kMode == kModePairFused;
+  static constexpr int kKStages =
+      kMode == kModePrepass ? 3
+      : (kMode == kModeFused ? 2 : ((kMode == kModePair || kMode == kModePairFused) ? 4 : (kMode == kModePairSplit ? 2 : 1)));
+  static constexpr int kVStages =
+      kMode == kModeSplit ? 1 : ((kMode == kModePair || kMode == kModePairFused) ? 4 : 2);
   // K stage: one tile (hi), or hi + lo; a CTA pair holds half of each
   static constexpr int kKStageBytes = (kSplit ? 2 * kTileBytes : kTileBytes) / (kPair ? 2 : 1);
   static constexpr int kVStageBytes = kPair ? kTileBytes / 2 : kTileBytes;
@@ -178,6 +186,7 @@ struct Params {
   int n_qblk;                  // CTAs per (b, h)
   int ctl_off;                 // byte offset of Ctl in the aligned dynamic smem
   float scale_log2;            // scale * log2(e)
+  float omega[64];             // rotary frequency of each channel pair (pairs past d/2 unused)
   const float2* table;
   __nv_bfloat16* out;
   float* lse;
@@ -303,14 +312,16 @@ struct RopeLane {
   int tab_base[4];   // entry of position 0 for each of the thread's pairs
   int tab_stride[4]; // entries per position step on that pair's axis
   int axis[4];       // 0 = t, 1 = h, 2 = w
+  float omega[4];    // rotary frequency of each pair
 };
 
 __device__ __forceinline__ RopeLane make_rope_lane(int c16, int half_t, int half_h, int half_w,
-                                                   int off_h, int off_w) {
+                                                   int off_h, int off_w, const float* omega) {
   RopeLane L;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const int pr = c16 * 4 + e;
+    L.omega[e] = omega[pr];
     if (pr < half_t) {
       L.axis[e] = 0; L.tab_base[e] = pr; L.tab_stride[e] = half_t;
     } else if (pr < half_t + half_h) {
@@ -325,7 +336,7 @@ __device__ __forceinline__ RopeLane make_rope_lane(int c16, int half_t, int half
 // Rotate the 4 pairs of one 16-byte chunk (bf16 in) of a token at grid position (pt,ph,pw)
 // and multiply by qs (scale*log2(e) for Q, 1 for K); returns the fp16 result and folds
 // |result| into amax.
-template <bool kLo>
+template <bool kLo, bool kSinCos = false>
 __device__ __forceinline__ uint4 rotate_chunk(uint4 x, const RopeLane& L, int pt, int ph, int pw,
                                               const float2* __restrict__ tab, float& amax,
                                               uint4* lo_out = nullptr, float qs = 1.f) {
@@ -334,7 +345,15 @@ __device__ __forceinline__ uint4 rotate_chunk(uint4 x, const RopeLane& L, int pt
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const int pos = L.axis[e] == 0 ? pt : (L.axis[e] == 1 ? ph : pw);
-    float2 cs = tab[L.tab_base[e] + pos * L.tab_stride[e]];
+    float2 cs;
+    if constexpr (kSinCos) {
+      // angle and its cosine/sine on the special-function unit instead of a table lookup in
+      // shared memory (absolute error ~1e-6 for the angles of a video grid, far below the
+      // fp16 rounding of the result)
+      __sincosf(static_cast<float>(pos) * L.omega[e], &cs.y, &cs.x);
+    } else {
+      cs = tab[L.tab_base[e] + pos * L.tab_stride[e]];
+    }
     cs.x *= qs;
     cs.y *= qs;
     const float x0 = __uint_as_float(w[e] << 16);
@@ -355,14 +374,14 @@ __device__ __forceinline__ uint4 rotate_chunk(uint4 x, const RopeLane& L, int pt
 // Rotate one 128-row tile in place (bf16 in, fp16 out, swizzled halves).  Thread t handles
 // chunk (t & 15) of rows (t >> 4) + 8*it; the 8 threads sharing a row hit 8 distinct
 // 16-byte bank groups.
-template <bool kLo>
+template <bool kLo, bool kSinCos = false, int kRows = kBM, int kHalfStride = kHalfBytes>
 __device__ __forceinline__ float rope_tile(const Params& p, const RopeLane& L, int t, uint8_t* tile,
                                            int n_first, const float2* __restrict__ tab, float qs,
                                            uint8_t* lo_tile = nullptr) {
   float amax = 0.f;
   const int c16 = t & 15;
   const int rsub = t >> 4;
-  const uint32_t chunk_off = (c16 >> 3) * kHalfBytes + rsub * 128 + (((c16 & 7) ^ rsub) << 4);
+  const uint32_t chunk_off = (c16 >> 3) * kHalfStride + rsub * 128 + (((c16 & 7) ^ rsub) << 4);
   int n = n_first + rsub;
   if (n >= p.N) return amax;
   int pt = n / p.HgWg;
@@ -370,10 +389,10 @@ __device__ __forceinline__ float rope_tile(const Params& p, const RopeLane& L, i
   int ph = rem / p.Wg;
   int pw = rem - ph * p.Wg;
 #pragma unroll 2
-  for (int it = 0; it < kBM / 8; ++it) {
+  for (int it = 0; it < kRows / 8; ++it) {
     if (n >= p.N) break;
     uint4* ptr = reinterpret_cast<uint4*>(tile + chunk_off + it * 1024);
-    *ptr = rotate_chunk<kLo>(*ptr, L, pt, ph, pw, tab, amax,
+    *ptr = rotate_chunk<kLo, kSinCos>(*ptr, L, pt, ph, pw, tab, amax,
                              kLo ? reinterpret_cast<uint4*>(lo_tile + chunk_off + it * 1024) : nullptr, qs);
     n += 8;
     pw += 8;
@@ -497,18 +516,22 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   // one arrival from each of rank 1's softmax warps.
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
   const bool leader = rank == 0u;
+  // With the fused K rotation the leader waits for the rotated tiles instead (its q/k "ready"
+  // barriers count one arrival from each of rank 1's RoPE warps), so rank 1 relays V only.
   const uint32_t full_count = (kPair && leader) ? 2u : 1u;
+  const uint32_t qk_full_count = kFusedK ? 1u : full_count;
+  const uint32_t ready_count = kPair ? 128 + 4 : 128;
 
   if (tid == 0) {
     for (int i = 0; i < kQTiles; ++i) {
-      mbar_init(smem_addr(&ctl->q_full[i]), full_count);
-      mbar_init(smem_addr(&ctl->q_ready[i]), 128);
+      mbar_init(smem_addr(&ctl->q_full[i]), qk_full_count);
+      mbar_init(smem_addr(&ctl->q_ready[i]), ready_count);
       mbar_init(smem_addr(&ctl->s_full[i]), 1);
       mbar_init(smem_addr(&ctl->p_ready[i]), kPair ? 128 + 4 : 128);
     }
     for (int s = 0; s < kKStages; ++s) {
-      mbar_init(smem_addr(&ctl->k_full[s]), full_count);
-      mbar_init(smem_addr(&ctl->k_ready[s]), 128);
+      mbar_init(smem_addr(&ctl->k_full[s]), qk_full_count);
+      mbar_init(smem_addr(&ctl->k_ready[s]), ready_count);
       mbar_init(smem_addr(&ctl->k_empty[s]), 1);
     }
     for (int s = 0; s < kVStages; ++s) {
@@ -624,13 +647,15 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       constexpr uint32_t kIdQK = idesc_f16kind_f32acc(2 * kBM, kBN, 0, 0);
       constexpr uint32_t kIdPV = idesc_f16kind_f32acc(2 * kBM, kD, 1, 1);
       const uint32_t tS0 = tmem + 0, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
-      bool ok = mbar_wait(smem_addr(&ctl->q_full[0]), 0, abort_flag, kSiteQReady) &&
-                mbar_wait(smem_addr(&ctl->q_full[1]), 0, abort_flag, kSiteQReady);
+      const uint64_t* qbar = kFusedK ? ctl->q_ready : ctl->q_full;
+      bool ok = mbar_wait(smem_addr(&qbar[0]), 0, abort_flag, kSiteQReady) &&
+                mbar_wait(smem_addr(&qbar[1]), 0, abort_flag, kSiteQReady);
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after_sync();
       auto k_wait = [&](int jj) {
-        return mbar_wait(smem_addr(&ctl->k_full[jj % kKStages]), (jj / kKStages) & 1, abort_flag,
-                                 kSiteKFull);
+        const int kss = jj % kKStages;
+        const uint32_t kbar = kFusedK ? smem_addr(&ctl->k_ready[kss]) : smem_addr(&ctl->k_full[kss]);
+        return mbar_wait(kbar, (jj / kKStages) & 1, abort_flag, kFusedK ? kSiteKReady : kSiteKFull);
       };
       if (ok && nkv > 0) ok = __all_sync(0xffffffffu, k_wait(0));
       for (int j = 0; ok && j < nkv; ++j) {
@@ -687,14 +712,16 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       // tells the leader, through one remote arrival per phase, that this CTA's Q tiles and
       // its half of each K/V stage have landed.
       bool ok = true;
-      for (int i = 0; ok && i < kQTiles; ++i) {
+      for (int i = 0; ok && i < kQTiles && !kFusedK; ++i) {
         ok = mbar_wait(smem_addr(&ctl->q_full[i]), 0, abort_flag, kSiteRelay);
         if (ok) mbar_arrive_remote(mapa_shared(smem_addr(&ctl->q_full[i]), 0));
       }
       for (int j = 0; ok && j < nkv && !p.withhold_kv; ++j) {
         const int ks = j % kKStages, vs = j % kVStages;
-        if (!(ok = mbar_wait(smem_addr(&ctl->k_full[ks]), (j / kKStages) & 1, abort_flag, kSiteRelay))) break;
-        mbar_arrive_remote(mapa_shared(smem_addr(&ctl->k_full[ks]), 0));
+        if constexpr (!kFusedK) {
+          if (!(ok = mbar_wait(smem_addr(&ctl->k_full[ks]), (j / kKStages) & 1, abort_flag, kSiteRelay))) break;
+          mbar_arrive_remote(mapa_shared(smem_addr(&ctl->k_full[ks]), 0));
+        }
         if (!(ok = mbar_wait(smem_addr(&ctl->v_full[vs]), (j / kVStages) & 1, abort_flag, kSiteRelay))) break;
         mbar_arrive_remote(mapa_shared(smem_addr(&ctl->v_full[vs]), 0));
       }
@@ -776,31 +803,50 @@ attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     regs_decrease<Lo::kRegsRope>();
     const int t = tid - 256;
     const float2* tab = (kFusedK && p.table_in_smem) ? tab_s : p.table;
-    const RopeLane L = make_rope_lane(t & 15, p.half_t, p.half_h, p.half_w, p.off_h, p.off_w);
+    const RopeLane L = make_rope_lane(t & 15, p.half_t, p.half_h, p.half_w, p.off_h, p.off_w, p.omega);
     bool ok = true;
     float amax = 0.f;
+    // This thread's rotated chunks are in place: make them visible to the tensor cores and
+    // arrive (rank 1 of a pair: one arrival per warp on the leader's barrier).
+    auto rotated = [&](uint64_t* bar) {
+      fence_proxy_async_smem();
+      if (!kPair || leader) {
+        mbar_arrive(smem_addr(bar));
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote_release(mapa_shared(smem_addr(bar), 0));
+      }
+    };
     for (int i = 0; i < kQTiles && ok && !p.q_prerot; ++i) {
       if (q_idx) {
         amax = fmaxf(amax, rope_gather_tile<kSplit>(p, L, t, smem + Lo::kOffQ + i * kTileBytes, q_idx,
                                                     q0 + i * kBM, b, h, tab, p.scale_log2,
                                                     smem + Lo::kOffQlo + i * kTileBytes));
       } else {
-        if (!(ok = mbar_wait(smem_addr(&ctl->q_full[i]), 0, abort_flag, kSiteQFull))) break;
-        amax = fmaxf(amax, rope_tile<kSplit>(p, L, t, smem + Lo::kOffQ + i * kTileBytes, q0 + i * kBM,
-                                             tab, p.scale_log2, smem + Lo::kOffQlo + i * kTileBytes));
+        // warp-uniform, so that a warp of rank 1 reaches its per-warp arrival together
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->q_full[i]), 0, abort_flag, kSiteQFull))))
+          break;
+        // CTA pairs with the fused K rotation take on-the-fly cosines/sines (their shared memory
+        // holds no table)
+        amax = fmaxf(amax, rope_tile<kSplit, kPair && kFusedK>(p, L, t, smem + Lo::kOffQ + i * kTileBytes, q0 + i * kBM,
+                                                    tab, p.scale_log2, smem + Lo::kOffQlo + i * kTileBytes));
       }
-      fence_proxy_async_smem();
-      mbar_arrive(smem_addr(&ctl->q_ready[i]));
+      rotated(&ctl->q_ready[i]);
     }
     if (kFusedK) {
       for (int j = 0; ok && j < nkv; ++j) {
         const int kt = cur.next();
         const int ks = j % kKStages;
-        if (!(ok = mbar_wait(smem_addr(&ctl->k_full[ks]), (j / kKStages) & 1, abort_flag, kSiteKFull)))
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->k_full[ks]), (j / kKStages) & 1,
+                                                      abort_flag, kSiteKFull))))
           break;
-        amax = fmaxf(amax, rope_tile<false>(p, L, t, smem + Lo::kOffK + ks * Lo::kKStageBytes, kt * kBN, tab, 1.f));
-        fence_proxy_async_smem();
-        mbar_arrive(smem_addr(&ctl->k_ready[ks]));
+        uint8_t* kst = smem + Lo::kOffK + ks * Lo::kKStageBytes;
+        if constexpr (kPair)   // this CTA's 64 keys of the tile, 64-channel halves 8 KB apart
+          amax = fmaxf(amax, rope_tile<false, true, kBN / 2, kHalfBytes / 2>(
+                                 p, L, t, kst, kt * kBN + static_cast<int>(rank) * (kBN / 2), tab, 1.f));
+        else
+          amax = fmaxf(amax, rope_tile<false, true>(p, L, t, kst, kt * kBN, tab, 1.f));
+        rotated(&ctl->k_ready[ks]);
       }
     }
     if (!(amax <= 65504.f)) atomicOr(&g_error_word, 2u);
@@ -968,7 +1014,7 @@ __device__ __forceinline__ void rope3d_prepass_body(const uint4* __restrict__ sr
   const uint32_t stride = gridDim.x * blockDim.x;
   uint32_t c = blockIdx.x * blockDim.x + threadIdx.x;
   const RopeLane L = make_rope_lane(static_cast<int>(c & 15), p.half_t, p.half_h, p.half_w,
-                                    p.off_h, p.off_w);
+                                    p.off_h, p.off_w, p.omega);
   const float qs = kQ ? p.scale_log2 : 1.f;
   float amax = 0.f;
   for (; c < n_chunks; c += stride) {
@@ -1002,6 +1048,13 @@ void fill_params(const Problem& pr, Params* p) {
   p->off_h = pr.T * pr.half_t;
   p->off_w = p->off_h + pr.Hg * pr.half_h;
   p->table_entries = pr.table_entries;
+  {
+    const int halves[3] = {pr.half_t, pr.half_h, pr.half_w};
+    int pair = 0;
+    for (int a = 0; a < 3; ++a)
+      for (int j = 0; j < halves[a] && pair < 64; ++j)
+        p->omega[pair++] = static_cast<float>(std::pow(pr.theta, -2.0 * j / (2 * halves[a])));
+  }
   p->scale_log2 = pr.scale * 1.4426950408889634f;
   p->table = pr.table;
   p->out = static_cast<__nv_bfloat16*>(pr.out);
@@ -1043,7 +1096,7 @@ cudaError_t launch_attn(const Problem& pr, Params p, const CUtensorMap* maps, cu
   const int tab_bytes = ((pr.table_entries * 8) + 15) & ~15;
   const int ctl_bytes = (static_cast<int>(sizeof(Ctl)) + 15) & ~15;
   int smem = Lo::kOffTab + tab_bytes + ctl_bytes + 1024;
-  if (kFusedK && smem <= kMaxDynSmem) {
+  if (kFusedK && !Lo::kPair && smem <= kMaxDynSmem) {
     p.table_in_smem = 1;
     p.ctl_off = Lo::kOffTab + tab_bytes;
   } else {
@@ -1111,9 +1164,9 @@ cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, KMod
   Params p;
   fill_params(pr, &p);
   CUtensorMap maps[6];
-  const bool fused = mode == KMode::kFused;
+  const bool fused = mode == KMode::kFused || mode == KMode::kPairFused;
   const bool split = mode == KMode::kSplit || mode == KMode::kPairSplit;
-  const bool pair = mode == KMode::kPair || mode == KMode::kPairSplit;
+  const bool pair = mode == KMode::kPair || mode == KMode::kPairSplit || mode == KMode::kPairFused;
   if (pair) {
     if (pr.q_index != nullptr || pr.kv_mask != nullptr) {
       *what = "CTA pairs take dense calls only";
@@ -1175,6 +1228,7 @@ cudaError_t launch_attn_bf16_sm103(const Problem& pr, EncodeTiledFn encode, KMod
     *what = "cuTensorMapEncodeTiled failed";
     return cudaErrorInvalidValue;
   }
+  if (fused && pair) return launch_attn<kModePairFused>(pr, p, maps, stream, what);
   if (fused) return launch_attn<kModeFused>(pr, p, maps, stream, what);
   if (pair && split) return launch_attn<kModePairSplit>(pr, p, maps, stream, what);
   if (pair) return launch_attn<kModePair>(pr, p, maps, stream, what);

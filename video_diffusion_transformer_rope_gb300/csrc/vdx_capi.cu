@@ -186,6 +186,7 @@ vdx_status prepare(const void* q, const void* k, const void* v, void* out, float
   if (s != VDX_OK) return s;
   p->table = tab;
   p->table_entries = entries;
+  p->theta = theta;
   return VDX_OK;
 }
 
@@ -222,8 +223,8 @@ static vdx_status attn_bf16(const void* q, const void* k, const void* v, void* o
   const int kernel = opt ? opt->kernel : VDX_KERNEL_DEFAULT;
   if (kernel != VDX_KERNEL_DEFAULT && kernel != VDX_KERNEL_SINGLE && kernel != VDX_KERNEL_PAIR)
     return fail(VDX_ERR_ARG, "unknown kernel %d", kernel);
-  if (kernel == VDX_KERNEL_PAIR && (fused || block_mask || q_index))
-    return fail(VDX_ERR_UNSUPPORTED, "VDX_KERNEL_PAIR takes dense calls with the K prepass only");
+  if (kernel == VDX_KERNEL_PAIR && (block_mask || q_index))
+    return fail(VDX_ERR_UNSUPPORTED, "VDX_KERNEL_PAIR takes dense calls only");
   // CTA pairs by default for dense calls with split operands (halving each CTA's K/V stages
   // lets its rings hold two stages instead of one: +16 % at N = 111600, +20 % at N = 32760)
   // and for long dense sequences with fp16 operands (N >= 65536, >= 512 key tiles per CTA): at
@@ -285,7 +286,7 @@ static vdx_status attn_bf16(const void* q, const void* k, const void* v, void* o
   vdx::EncodeTiledFn enc = nullptr;
   if ((s = get_encode(&enc)) != VDX_OK) return s;
   const char* what = nullptr;
-  const vdx::KMode km = fused ? vdx::KMode::kFused
+  const vdx::KMode km = fused ? (pair ? vdx::KMode::kPairFused : vdx::KMode::kFused)
                               : (split ? (pair ? vdx::KMode::kPairSplit : vdx::KMode::kSplit)
                                        : (pair ? vdx::KMode::kPair : vdx::KMode::kPrepass));
   cudaError_t e = vdx::launch_attn_bf16_sm103(p, enc, km, ws, q_pre, static_cast<cudaStream_t>(stream),

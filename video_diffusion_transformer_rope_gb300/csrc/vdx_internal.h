@@ -19,6 +19,7 @@ struct Problem {
   float* lse;           // may be nullptr
   int B, H, T, Hg, Wg, N, d;
   int half_t, half_h, half_w;   // rotary pairs per axis
+  double theta = 10000.0;       // rotary base
   float scale;
   const float2* table;
   int table_entries;
@@ -51,7 +52,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 // With rotate_q_in_prepass (kPrepass / kSplit, no query subset) the prepass also rotates Q
 // (multiplied by scale*log2(e)) into the workspace after K, and the attention kernel loads
 // it rotated; otherwise every CTA rotates its Q tiles in shared memory.
-enum class KMode { kPrepass, kFused, kSplit, kPair, kPairSplit };
+enum class KMode { kPrepass, kFused, kSplit, kPair, kPairSplit, kPairFused };
 cudaError_t launch_attn_bf16_sm103(const Problem& p, EncodeTiledFn encode, KMode mode,
                                    void* workspace, bool rotate_q_in_prepass, cudaStream_t stream,
                                    const char** what);

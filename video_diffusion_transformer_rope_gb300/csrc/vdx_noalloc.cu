@@ -170,6 +170,7 @@ extern "C" vdx_status vdx_rope3d_attn_noalloc(const void* q, const void* k, cons
   p.q = q; p.k = k; p.v = v; p.out = out; p.lse = lse;
   p.B = B; p.H = H; p.T = T; p.Hg = Hgrid; p.Wg = Wgrid; p.N = static_cast<int>(N); p.d = d;
   p.half_t = sec_t / 2; p.half_h = sec_h / 2; p.half_w = sec_w / 2;
+  p.theta = theta;
   p.scale = scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
   p.table = table;
   p.table_entries = static_cast<int>(entries);
