@@ -355,12 +355,13 @@ def _e2e_leg(w, q, k, v, out, lse, hq, hk, hv, call, stream, dev, barrier, max_o
 
 
 def _kernel_used(args, w):
-    """Which attention kernel runs the timed calls (the library's default rule for dense calls
-    with the K prepass: CTA pairs for split operands, or for fp16 operands with N >= 65536)."""
+    """Which attention kernel runs the timed calls (the library's default rule for dense calls:
+    CTA pairs with the fused K rotation, with split operands, or with fp16 operands and
+    N >= 65536)."""
     if args.kernel != "default":
         return args.kernel
-    dense = not args.window and not args.subset and args.k_rope == "prepass"
-    return "pair" if dense and (w.qk == "split" or w.N >= 65536) else "single"
+    dense = not args.window and not args.subset
+    return "pair" if dense and (args.k_rope == "fused" or w.qk == "split" or w.N >= 65536) else "single"
 
 
 def run_ours(args, w):
@@ -500,7 +501,7 @@ def run_ours(args, w):
                          "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)",
                          "frac_of_sustained": (tflops_rank / peak_sus) if peak_sus else None,
                          "kernel": (f"attn_fwd_sm103, {_kernel_used(args, w)} (+ rope3d_qk_prepass)"
-                                    if args.k_rope == "prepass" else "attn_fwd_sm103 (fused K rotation)")},
+                                    if args.k_rope == "prepass" else f"attn_fwd_sm103, {_kernel_used(args, w)}, fused K rotation")},
             "cpu_baseline": cpu,
             "clocks": clocks,
         }

@@ -64,8 +64,9 @@ typedef enum {
                                  half the speed; needs the K prepass and twice its workspace  */
 
 /* Which attention kernel runs a dense bf16 call. */
-#define VDX_KERNEL_DEFAULT 0  /* VDX_KERNEL_PAIR where it applies with VDX_QK_SPLIT, or with
-                                 VDX_QK_FP16 and N >= 65536; else VDX_KERNEL_SINGLE              */
+#define VDX_KERNEL_DEFAULT 0  /* VDX_KERNEL_PAIR for dense calls with VDX_K_ROPE_FUSED, with
+                                 VDX_QK_SPLIT, or with VDX_QK_FP16 and N >= 65536; else
+                                 VDX_KERNEL_SINGLE                                                */
 #define VDX_KERNEL_SINGLE 1   /* one CTA per 256 query rows, each streaming whole K/V tiles          */
 #define VDX_KERNEL_PAIR 2     /* clusters of two CTAs: each holds half of every K/V tile and the pair
                                  multiplies both CTAs' 512 query rows with CTA-pair MMAs; dense

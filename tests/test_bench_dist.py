@@ -57,6 +57,7 @@ def test_kernel_choice_and_stored_traffic_follow_the_library_rule():
     assert bench._kernel_used(args, configs.WAN14B_720P) == "pair"
     assert bench._kernel_used(args, configs.LONG_STRESS) == "pair"
     assert bench._kernel_used(args, configs.WAN13B_480P) == "single"
+    assert bench._kernel_used(argparse.Namespace(**{**vars(args), "k_rope": "fused"}), configs.WAN13B_480P) == "pair"
     assert bench._kernel_used(argparse.Namespace(**{**vars(args), "window": "2,6,10"}), configs.WAN14B_720P) == "single"
     assert bench._kernel_used(argparse.Namespace(**{**vars(args), "kernel": "single"}), configs.WAN14B_720P) == "single"
     t = bench._traffic_per_launch("wan14b_720p", "pair")

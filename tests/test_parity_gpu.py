@@ -67,8 +67,9 @@ K_MODES = {"prepass": vdx.K_ROPE_PREPASS, "fused": vdx.K_ROPE_FUSED}
 @pytest.mark.parametrize("mode", sorted(K_MODES))
 @pytest.mark.parametrize("grid", BF16_GRIDS, ids=lambda g: "x".join(map(str, g)))
 def test_bf16_small_shapes(grid, mode):
+    # the one-CTA kernel (fused calls default to CTA pairs, tested below)
     w = dataclasses.replace(configs.WAN13B_480P, B=2, H=3, T=grid[0], Hg=grid[1], Wg=grid[2], seed=21)
-    mx, mean, lerr = _full_compare(w, k_rope=K_MODES[mode])
+    mx, mean, lerr = _full_compare(w, k_rope=K_MODES[mode], kernel=vdx.KERNEL_SINGLE)
     assert mx <= BF16_MAX and mean <= BF16_MEAN and lerr <= LSE_TOL, (mx, mean, lerr)
 
 
@@ -337,7 +338,7 @@ def test_long_rows_with_and_without_a_ragged_tile(grid, k_rope):
     # N = 255*128 (no ragged key tile) and N = 256*128 + 1 (a last tile of one key); the prepass
     # mode rotates Q in the prepass, the fused mode in every CTA.
     w = dataclasses.replace(configs.WAN13B_480P, B=1, H=2, T=grid[0], Hg=grid[1], Wg=grid[2], seed=34)
-    kw = {"prepass": {}, "fused": {"k_rope": vdx.K_ROPE_FUSED},
+    kw = {"prepass": {}, "fused": {"k_rope": vdx.K_ROPE_FUSED, "kernel": vdx.KERNEL_SINGLE},
           "fused_pair": {"k_rope": vdx.K_ROPE_FUSED, "kernel": vdx.KERNEL_PAIR}}[k_rope]
     mx, mean, lerr, stats = _sampled_compare(w, rows=256, **kw)
     _assert_sampled(w, mx, mean, lerr, stats)

@@ -94,7 +94,7 @@ def rope3d_attn(q, k, v, grid, sections=(0, 0, 0), theta=10000.0, scale=0.0, out
     for logits in the hundreds); workspace is an optional CUDA tensor of at least
     workspace_bytes(...) bytes for the prepass (None: the library's own per-device buffer);
     kernel selects KERNEL_SINGLE (one CTA per 256 query rows) or KERNEL_PAIR (CTA pairs sharing
-    each K/V tile; dense fp16 calls only), KERNEL_DEFAULT the library's choice.
+    each K/V tile; dense calls only), KERNEL_DEFAULT the library's choice.
 
     Returns (out [B, N, H, d] in the input dtype, lse [B, H, N] float32 or None).  Enqueued on
     `stream` (default: torch's current stream); call sync_check() to surface device errors.

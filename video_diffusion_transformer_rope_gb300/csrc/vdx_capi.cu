@@ -231,10 +231,12 @@ static vdx_status attn_bf16(const void* q, const void* k, const void* v, void* o
   // the same power pairs run ~7 % higher clocks (half the shared-memory operand reads and
   // L2->SM traffic per CTA), which outweighs their longer cross-SM signalling there (+0.8 % at
   // N = 75600); at N = 32760 they measured -1.8 % to +0.2 %, so shorter fp16 calls keep one CTA.
+  // With the fused K rotation pairs halve each CTA's rotation work: 1.58x faster at N = 32760
+  // and 75600 (H = 12 and 40).
   const long long n_tokens = static_cast<long long>(T) * Hgrid * Wgrid;
   const bool pair = kernel == VDX_KERNEL_PAIR ||
-                    (kernel == VDX_KERNEL_DEFAULT && !fused && !block_mask && !q_index &&
-                     (split || n_tokens >= 65536));
+                    (kernel == VDX_KERNEL_DEFAULT && !block_mask && !q_index &&
+                     (fused || split || n_tokens >= 65536));
   if (fused && split)
     return fail(VDX_ERR_UNSUPPORTED, "VDX_QK_SPLIT needs the K prepass (k_rope = VDX_K_ROPE_PREPASS)");
   vdx::Problem p{};
