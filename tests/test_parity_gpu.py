@@ -233,13 +233,13 @@ def test_bf16_deterministic_and_guard_bands():
     assert none is None and torch.equal(out2, out)
 
 
-def _sampled_compare(w, rows=512, **kw):
+def _sampled_compare(w, rows=512, sel=None, **kw):
     """Sampled rows of one full-size call against the oracle: (out max-abs, out mean-abs,
     lse max-abs, stats) with stats holding the relative guards and, for a stress workload,
-    the errors on its outlier-token rows alone."""
+    the errors on its outlier-token rows alone.  `sel` overrides the sampled (b, h, n) rows."""
     q, k, v = synth.make_qkv(w, device="cuda")
     out, lse = _run(w, q, k, v, **kw)
-    sel = synth.sample_rows(w, rows)
+    sel = synth.sample_rows(w, rows) if sel is None else sel
     ref_o, ref_l = O.rope3d_attention_rows(q, k, v, (w.T, w.Hg, w.Wg), sel, w.sections, w.theta)
     b = torch.tensor([r[0] for r in sel], device="cuda")
     h = torch.tensor([r[1] for r in sel], device="cuda")
@@ -275,6 +275,28 @@ def _assert_sampled(w, mx, mean, lerr, stats):
         assert stats["outlier_rows"] == round(0.001 * w.N), stats
         assert (stats["outlier_out_max"] <= BF16_MAX and stats["outlier_out_mean"] <= BF16_MEAN and
                 stats["outlier_lse_max"] <= LSE_TOL and stats["outlier_rel_mean"] <= REL_MEAN), stats
+
+
+# Tensors of more than 2^31 elements: B = 2, H = 40, grid 59 x 45 x 80 (N = 212400) is
+# 2.17e9 elements (4.35 GB of bf16) per tensor, so the rows of batch entry 1 sit past element
+# offset 2^31 in q, k, v, out and the prepass workspace.  Rows of three heads (both batch
+# entries, first and last heads), including each head's first and last tokens.
+@pytest.mark.parametrize("k_rope", ["prepass", "fused"])
+def test_tensors_beyond_2_31_elements_sampled(k_rope):
+    w = dataclasses.replace(configs.WAN14B_720P, B=2, H=40, T=59, Hg=45, Wg=80, seed=61)
+    assert w.B * w.N * w.H * w.d > 2 ** 31
+    rng = np.random.default_rng(61)
+    sel = []
+    for b, h in [(1, 39), (1, 0), (0, 20)]:
+        ns = [0, 1, w.N // 2, w.N - 2, w.N - 1] + list(rng.integers(0, w.N, 35))
+        sel += [(b, h, int(n)) for n in ns]
+    kw = {} if k_rope == "prepass" else {"k_rope": vdx.K_ROPE_FUSED}
+    try:
+        mx, mean, lerr, stats = _sampled_compare(w, sel=sel, **kw)
+    finally:
+        torch.cuda.empty_cache()
+    print(f"2^31+ elements ({k_rope}): out max {mx:.3e} mean {mean:.3e} lse max {lerr:.3e} {stats}")
+    _assert_sampled(w, mx, mean, lerr, stats)
 
 
 @pytest.mark.parametrize("w", [configs.WAN13B_480P, configs.WAN14B_480P, configs.WAN14B_720P,
