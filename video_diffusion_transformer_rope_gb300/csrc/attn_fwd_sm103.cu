@@ -19,7 +19,8 @@
 //   WG3  warp 12     TMA producer: Q tiles once, then K/V tiles through the rings
 //        warp 13     tcgen05 MMA issuer (the whole warp runs the loop, one elected lane
 //                    issues) and TMEM owner (in a CTA pair: rank 0 only)
-//        warp 14     rank 1 of a CTA pair: relays its landed Q/K/V halves to rank 0
+//        warp 14     rank 1 of a CTA pair: relays its landed Q/K/V halves to rank 0 (V only
+//                    with the fused K rotation, where rank 1's WG2 signals its rotated tiles)
 //        warp 15     idle
 //
 // K modes.  Prepass (default): a separate kernel rotates K once per token into an fp16
@@ -28,7 +29,10 @@
 // query subset (gathered rows), the fused-K mode and the no-allocation entry have WG2 rotate
 // each CTA's Q tiles.
 // Fused: TMA brings raw bf16 K and WG2 rotates each K tile in shared memory before the MMA
-// reads it (every CTA of a head repeats this for every K tile).
+// reads it (every CTA of a head repeats this for every K tile).  On CTA pairs (the default for
+// fused calls) each CTA rotates only its own 64 keys of every K tile, with cosines and sines
+// from the special-function unit (no table in shared memory), and rank 1's WG2 signals the
+// rotated half to rank 0, whose MMA warp waits for both halves before it issues.
 // Split (precise): as prepass, but every rotated Q/K value x is kept as two fp16 numbers,
 // hi = fp16(x) and lo = fp16(x - hi), and S = Qhi Khi^T + Qhi Klo^T + Qlo Khi^T (about 22
 // significant bits per operand instead of 11) for inputs whose logits reach the hundreds.
