@@ -74,9 +74,9 @@ def _source_hash():
     return hashlib.sha256(src.encode()).hexdigest()[:16]
 
 
-def _traffic_per_launch(workload, kernel):
+def _traffic_per_launch(workload, kernel, k_rope="prepass"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel
-    (same source, same kernel variant, same workload)."""
+    (same source, same kernel variant and K rotation mode, same workload)."""
     try:
         kv = {}
         with open(TRAFFIC_FILE) as f:
@@ -85,7 +85,7 @@ def _traffic_per_launch(workload, kernel):
                     key, val = line.split(":", 1)
                     kv[key.strip()] = val.strip()
         if (kv.get("kernel_source_sha256_16") != _source_hash() or kv.get("workload") != workload or
-                kv.get("kernel", "single") != kernel):
+                kv.get("kernel", "single") != kernel or kv.get("k_rope", "prepass") != k_rope):
             return None
         return float(kv["dram_bytes_per_launch"])
     except Exception:
@@ -477,7 +477,7 @@ def run_ours(args, w):
     tflops_rank = job_tflops(work, ms, 1)
     value = job_tflops(work, ms, ws)
     peak, peak_sus, peak_src = _peaks()
-    traffic = _traffic_per_launch(w.name, _kernel_used(args, w))
+    traffic = _traffic_per_launch(w.name, _kernel_used(args, w), args.k_rope)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.window and not args.subset:

@@ -50,7 +50,7 @@ def test_single_rank_is_identity():
 def test_kernel_choice_and_stored_traffic_follow_the_library_rule():
     # bench.py names the attention kernel a run uses with the library's default rule (CTA pairs
     # for split operands, or for fp16 operands with N >= 65536) and reports the stored DRAM
-    # traffic only for the kernel variant and workload it was captured on.
+    # traffic only for the kernel variant, K rotation mode and workload it was captured on.
     import argparse
     from video_diffusion_transformer_rope_gb300 import configs
     args = argparse.Namespace(kernel="default", window=None, subset=None, k_rope="prepass")
@@ -64,3 +64,4 @@ def test_kernel_choice_and_stored_traffic_follow_the_library_rule():
     assert t is None or 6.2e9 <= t <= 9e9          # algorithmic bytes are 6.22 GB per launch
     assert bench._traffic_per_launch("wan14b_720p", "single") is None
     assert bench._traffic_per_launch("wan1.3b_480p", "pair") is None
+    assert bench._traffic_per_launch("wan14b_720p", "pair", "fused") is None   # another K mode
